@@ -1,0 +1,36 @@
+"""Float64 CPU oracle for fused RMSNorm forward and backward.
+
+TEST INFRASTRUCTURE ONLY.  ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import it; the library under
+``bwd_rms_norm_gb300/`` never does, and the two share no code.
+
+Parity status of each function (what pins it is in ``tests/test_oracle.py``):
+
+* ``rounding.round_to`` -- pinned: the worked example and the two-million
+  sample count of "Den dolda avrundningen i RMSNorm", exhaustive checks of
+  every bf16 and fp16 value and midpoint, numpy's float64-to-float16 cast and
+  torch's float32-to-bfloat16 cast.
+* ``rms_norm.forward`` / ``forward_exact`` -- pinned: torch's CPU ``rms_norm``
+  in float64 (the plain definition), torch's CPU bf16 ``rms_norm`` (single
+  rounding after a float32 multiply), closed forms for one-element and
+  constant rows, scale invariance, the Gemma gain identity.
+* ``rms_norm.backward`` / ``backward_exact`` -- pinned: central finite
+  differences of sum(dy * y) in float64, torch autograd through CPU
+  ``rms_norm`` in float64, the orthogonality of dx to x at eps = 0.
+"""
+from .rounding import FORMATS, max_finite, round_to, ulp_distance  # noqa: F401
+from .rms_norm import (  # noqa: F401
+    BF16,
+    F16,
+    F32,
+    ROUND_ONCE,
+    ROUND_TWICE,
+    backward,
+    backward_exact,
+    eps_value,
+    forward,
+    forward_exact,
+    gain,
+    rstd_exact,
+    store_y,
+)

@@ -1,0 +1,133 @@
+"""Seeded synthetic inputs for fused RMSNorm forward and backward.
+
+This module holds shapes, value distributions and seeds, nothing of the
+normalisation itself, so that the oracle and the CUDA path can both draw
+their inputs from it without sharing any arithmetic of the method.
+
+Every tensor is drawn on the CPU with its own ``torch.Generator`` seeded
+``seed + k`` (k = 0 for x, 1 for gamma, 2 for dy), in float32, scaled and
+shifted, and then rounded once (round to nearest even) to the storage type.
+Both sides therefore receive the same already-rounded values, which is the
+comparison the precision page recommends ("Den dolda avrundningen i RMSNorm",
+section "Ge testet samma precision som modellen").  A normal distribution
+is written ``("normal", mean, variance)``: the second parameter is the
+variance, so N(0, 64) has standard deviation 8.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, Optional, Tuple
+
+import torch
+
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+ELEMENT_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
+
+Dist = Tuple[str, float, float]
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    rows: int
+    hidden: int
+    dtype: str              # "f32" | "bf16" | "f16"
+    eps: float
+    offset: int             # 1: Gemma gain 1 + gamma
+    cast_mode: str          # "round_once" | "round_twice"
+    x_dist: Dist
+    gamma_dist: Dist
+    dy_dist: Dist
+    seed: int = 0
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+    @property
+    def elem_bytes(self) -> int:
+        return ELEMENT_BYTES[self.dtype]
+
+    def fwd_bytes(self) -> int:
+        """Bytes the forward must move: read x and gamma, write y and rstd."""
+        s, r, n = self.elem_bytes, self.rows, self.hidden
+        return 2 * r * n * s + 4 * r + n * s
+
+    def bwd_bytes(self) -> int:
+        """Bytes the backward must move: read dy, x, gamma and rstd, write dx
+        and the float32 weight gradient."""
+        s, r, n = self.elem_bytes, self.rows, self.hidden
+        return 3 * r * n * s + 4 * r + n * s + 4 * n
+
+    def step_bytes(self) -> int:
+        return self.fwd_bytes() + self.bwd_bytes()
+
+
+_N01: Dist = ("normal", 0.0, 1.0)
+_U0911: Dist = ("uniform", 0.9, 1.1)
+
+# Fixed fp32 case, small enough for the oracle to finish in well under a second.
+FP32_256x1024 = Workload("fp32_256x1024", 256, 1024, "f32", 1e-6, 0, "round_once",
+                         _N01, _U0911, _N01)
+# Llama-shaped bf16 activation: 4 sequences of 1024 tokens, hidden 4096.
+LLAMA_BF16_4096x4096 = Workload("llama_bf16_4096x4096", 4096, 4096, "bf16", 1e-5, 0,
+                                "round_once", _N01, _U0911, _N01)
+# Gemma-shaped bf16 activation with the 1 + gamma gain.
+GEMMA_BF16_8192x3072 = Workload("gemma_bf16_8192x3072", 8192, 3072, "bf16", 1e-6, 1,
+                                "round_once", ("normal", 0.0, 2.0),
+                                ("normal", 0.0, 0.1), _N01)
+# fp16 sweep over hidden sizes; x has variance 64 so that a sum of squares in
+# fp16 would overflow.
+FP16_SWEEP_HIDDEN = (1024, 2048, 4096, 8192, 16384, 32768)
+
+
+def fp16_sweep(hidden: int, x_var: float = 64.0) -> Workload:
+    tag = "" if x_var == 64.0 else f"_var{int(x_var)}"
+    return Workload(f"fp16_4096x{hidden}{tag}", 4096, hidden, "f16", 1e-6, 0,
+                    "round_once", ("normal", 0.0, x_var), _U0911, _N01)
+
+
+def large_bf16(cast_mode: str) -> Workload:
+    tag = "once" if cast_mode == "round_once" else "twice"
+    return Workload(f"large_bf16_16384x8192_{tag}", 16384, 8192, "bf16", 1e-5, 0,
+                    cast_mode, _N01, _U0911, _N01)
+
+
+def all_workloads() -> Dict[str, Workload]:
+    ws = [FP32_256x1024, LLAMA_BF16_4096x4096, GEMMA_BF16_8192x3072]
+    ws += [fp16_sweep(n) for n in FP16_SWEEP_HIDDEN]
+    ws += [large_bf16("round_once"), large_bf16("round_twice")]
+    return {w.name: w for w in ws}
+
+
+def _draw(shape, dist: Dist, seed: int) -> torch.Tensor:
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    kind, a, b = dist
+    if kind == "normal":
+        t = torch.randn(shape, generator=gen, dtype=torch.float32)
+        return t * math.sqrt(b) + a
+    if kind == "uniform":
+        t = torch.rand(shape, generator=gen, dtype=torch.float32)
+        return t * (b - a) + a
+    if kind == "zeros":
+        return torch.zeros(shape, dtype=torch.float32)
+    raise ValueError(f"unknown distribution {kind!r}")
+
+
+def make_inputs(w: Workload, rows: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """CPU tensors x [rows, hidden], gamma [hidden], dy [rows, hidden] in the
+    workload's storage type.  ``rows`` overrides the row count (the first
+    ``rows`` rows of the same draw are *not* guaranteed: a different count is
+    a different draw)."""
+    r = w.rows if rows is None else rows
+    dt = DTYPES[w.dtype]
+    x = _draw((r, w.hidden), w.x_dist, w.seed + 0).to(dt)
+    gamma = _draw((w.hidden,), w.gamma_dist, w.seed + 1).to(dt)
+    dy = _draw((r, w.hidden), w.dy_dist, w.seed + 2).to(dt)
+    return {"x": x, "gamma": gamma, "dy": dy}
+
+
+def as_float64(t: torch.Tensor):
+    """The values of a CPU tensor as a float64 numpy array (exact widening)."""
+    return t.detach().to("cpu").to(torch.float64).numpy()
