@@ -1,0 +1,191 @@
+"""Python binding of the GB300 fused RMSNorm library (librms_norm_gb300.so).
+
+Argument marshalling only: every step of the forward and the backward runs
+in the library's CUDA kernels.  PyTorch supplies device memory and the
+current CUDA stream.  There is no CPU fallback: without the built library,
+or with tensors that are not on a CUDA device, every call raises.
+
+The functions carry the names of the C entry points declared in
+``include/rms_norm.h``:
+
+* ``rms_norm_fwd(x, gamma, eps, offset=0, cast_mode="round_once")``
+  -> ``(y, rstd)``
+* ``rms_norm_bwd(dy, x, gamma, rstd, offset=0)`` -> ``(dx, dw)``
+* ``rms_norm_bwd_workspace_size(rows, hidden, dtype)``
+* ``rms_norm_status_string(status)``
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+LIB_NAME = "librms_norm_gb300.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
+
+# Values of the C enums (include/rms_norm.h).
+RMSN_F32, RMSN_BF16, RMSN_F16 = 0, 1, 2
+RMSN_ROUND_ONCE, RMSN_ROUND_TWICE = 0, 1
+RMSN_OK = 0
+RMSN_MAX_HIDDEN = 65536
+RMSN_MAX_PARTIALS = 1024
+
+DTYPE_CODES = {torch.float32: RMSN_F32, torch.bfloat16: RMSN_BF16, torch.float16: RMSN_F16}
+CAST_MODES = {"round_once": RMSN_ROUND_ONCE, "round_twice": RMSN_ROUND_TWICE}
+
+EXPORTED = (
+    "rms_norm_fwd",
+    "rms_norm_bwd_workspace_size",
+    "rms_norm_bwd",
+    "rms_norm_status_string",
+    "rms_norm_last_cuda_error",
+    "rms_norm_last_launch_count",
+)
+
+
+class RMSNormError(RuntimeError):
+    """A C entry point returned an error status."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: status {status} ({rms_norm_status_string(status)})")
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library and declare the C signatures (once)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it first (python -m bwd_rms_norm_gb300.build)")
+    lib = ctypes.CDLL(path)
+    P, I64, I, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.rms_norm_fwd.argtypes = [P, P, P, P, I64, I64, F, I, I, I, P]
+    lib.rms_norm_fwd.restype = I
+    lib.rms_norm_bwd_workspace_size.argtypes = [I64, I64, I]
+    lib.rms_norm_bwd_workspace_size.restype = SZ
+    lib.rms_norm_bwd.argtypes = [P, P, P, P, P, P, I64, I64, I, I, P, SZ, P]
+    lib.rms_norm_bwd.restype = I
+    lib.rms_norm_status_string.argtypes = [I]
+    lib.rms_norm_status_string.restype = ctypes.c_char_p
+    lib.rms_norm_last_cuda_error.argtypes = []
+    lib.rms_norm_last_cuda_error.restype = I
+    lib.rms_norm_last_launch_count.argtypes = []
+    lib.rms_norm_last_launch_count.restype = I
+    _lib = lib
+    return lib
+
+
+def rms_norm_status_string(status: int) -> str:
+    return load_library().rms_norm_status_string(int(status)).decode()
+
+
+def rms_norm_bwd_workspace_size(rows: int, hidden: int, dtype) -> int:
+    """Bytes of workspace ``rms_norm_bwd`` needs (``dtype`` a torch dtype or
+    a C code)."""
+    code = DTYPE_CODES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load_library().rms_norm_bwd_workspace_size(int(rows), int(hidden), code))
+
+
+def last_launch_count() -> int:
+    """Kernels enqueued by the last successful call on this thread."""
+    return int(load_library().rms_norm_last_launch_count())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None or t.numel() == 0 else t.data_ptr()
+
+
+def _stream_handle(device: torch.device, stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _check_cuda(name: str, t: torch.Tensor) -> None:
+    if not t.is_cuda:
+        raise RuntimeError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if not t.is_contiguous():
+        raise RuntimeError(f"{name} must be contiguous")
+
+
+def _as_rows(x: torch.Tensor) -> Tuple[int, int]:
+    if x.dim() < 1:
+        raise RuntimeError("x must have at least one dimension")
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden > 0 else 0
+    return rows, hidden
+
+
+def rms_norm_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float, offset: int = 0,
+                 cast_mode: str = "round_once", y: Optional[torch.Tensor] = None,
+                 rstd: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None):
+    """Forward over the last dimension of ``x``; returns ``(y, rstd)`` with
+    ``y`` shaped like ``x`` and ``rstd`` fp32 of shape ``x.shape[:-1]``."""
+    lib = load_library()
+    _check_cuda("x", x)
+    _check_cuda("gamma", gamma)
+    if gamma.dtype != x.dtype:
+        raise RuntimeError("gamma must have the dtype of x")
+    rows, hidden = _as_rows(x)
+    if gamma.numel() != hidden:
+        raise RuntimeError("gamma must have hidden elements")
+    if y is None:
+        y = torch.empty_like(x)
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _check_cuda("y", y)
+    _check_cuda("rstd", rstd)
+    with torch.cuda.device(x.device):
+        st = lib.rms_norm_fwd(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), rows, hidden,
+                              float(eps), int(offset), DTYPE_CODES[x.dtype],
+                              CAST_MODES[cast_mode], _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_fwd", st)
+    return y, rstd
+
+
+def rms_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: torch.Tensor,
+                 offset: int = 0, dx: Optional[torch.Tensor] = None,
+                 dw: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None):
+    """Backward; returns ``(dx, dw)`` with ``dw`` fp32 of shape ``[hidden]``.
+    ``workspace`` (a byte or float tensor of at least
+    ``rms_norm_bwd_workspace_size`` bytes) is allocated when not given."""
+    lib = load_library()
+    for name, t in (("dy", dy), ("x", x), ("gamma", gamma), ("rstd", rstd)):
+        _check_cuda(name, t)
+    if dy.dtype != x.dtype or gamma.dtype != x.dtype:
+        raise RuntimeError("dy, x and gamma must share one dtype")
+    if rstd.dtype != torch.float32:
+        raise RuntimeError("rstd must be float32")
+    if dy.shape != x.shape:
+        raise RuntimeError("dy must have the shape of x")
+    rows, hidden = _as_rows(x)
+    if rstd.numel() != rows or gamma.numel() != hidden:
+        raise RuntimeError("rstd must have one value per row and gamma hidden values")
+    code = DTYPE_CODES[x.dtype]
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    need = int(lib.rms_norm_bwd_workspace_size(rows, hidden, code))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check_cuda("dx", dx)
+    _check_cuda("dw", dw)
+    _check_cuda("workspace", workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(x.device):
+        st = lib.rms_norm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dw),
+                              rows, hidden, int(offset), code, workspace.data_ptr(), ws_bytes,
+                              _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_bwd", st)
+    return dx, dw

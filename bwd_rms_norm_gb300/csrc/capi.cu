@@ -1,0 +1,177 @@
+// C ABI of the fused RMSNorm library: argument validation and dispatch.
+// Every check runs on the host before anything is enqueued.
+#include <math.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "launch.h"
+#include "rms_norm.h"
+
+namespace rmsn {
+
+namespace {
+thread_local int t_last_cuda_error = 0;
+thread_local int t_last_launches = 0;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+struct OccEntry {
+  const void* func;
+  int block;
+  size_t smem;
+  int device;
+  int value;
+};
+std::mutex g_occ_mutex;
+OccEntry g_occ[256];
+int g_occ_n = 0;
+
+int elem_bytes(int dtype) { return dtype == RMSN_F32 ? 4 : 2; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return RMSN_ERR_CUDA;
+}
+}  // namespace
+
+int sm_count(int device) {
+  if (device >= 0 && device < kMaxDevices) {
+    int v = g_sm_count[device].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0)
+    n = 1;
+  if (device >= 0 && device < kMaxDevices) g_sm_count[device].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int max_blocks_per_sm(const void* func, int block, size_t smem) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    for (int i = 0; i < g_occ_n; ++i)
+      if (g_occ[i].func == func && g_occ[i].block == block && g_occ[i].smem == smem &&
+          g_occ[i].device == dev)
+        return g_occ[i].value;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, block, smem) != cudaSuccess) n = 1;
+  if (n < 1) n = 1;
+  std::lock_guard<std::mutex> lock(g_occ_mutex);
+  if (g_occ_n < 256) g_occ[g_occ_n++] = OccEntry{func, block, smem, dev, n};
+  return n;
+}
+
+}  // namespace rmsn
+
+using namespace rmsn;
+
+extern "C" {
+
+int rms_norm_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t rows,
+                 int64_t hidden, float eps, int offset, int dtype, int cast_mode,
+                 void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if ((offset != 0 && offset != 1) || (cast_mode != RMSN_ROUND_ONCE && cast_mode != RMSN_ROUND_TWICE))
+    return RMSN_ERR_ARG;
+  if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
+    return RMSN_ERR_SHAPE;
+  if (!(eps >= 0.f) || isinf(eps)) return RMSN_ERR_EPS;
+  t_last_launches = 0;
+  if (rows == 0) return RMSN_OK;
+  if (!x || !gamma || !y || !rstd) return RMSN_ERR_NULL;
+
+  const int s = elem_bytes(dtype);
+  FwdArgs a;
+  a.x = x;
+  a.gamma = gamma;
+  a.y = y;
+  a.rstd = rstd;
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.eps = eps;
+  a.offset = offset;
+  a.twice = cast_mode == RMSN_ROUND_TWICE ? 1 : 0;
+  a.vec_ok = ((hidden * s) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y);
+  int launches = 0;
+  cudaError_t e = launch_fwd(dtype, a, static_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = launches;
+  return RMSN_OK;
+}
+
+size_t rms_norm_bwd_workspace_size(int64_t rows, int64_t hidden, int dtype) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return 0;
+  if (rows <= 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN) return 0;
+  const int64_t parts = rows < RMSN_MAX_PARTIALS ? rows : RMSN_MAX_PARTIALS;
+  return (size_t)parts * (size_t)hidden * sizeof(float);
+}
+
+int rms_norm_bwd(const void* dy, const void* x, const void* gamma, const float* rstd, void* dx,
+                 float* dw, int64_t rows, int64_t hidden, int offset, int dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (offset != 0 && offset != 1) return RMSN_ERR_ARG;
+  if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
+    return RMSN_ERR_SHAPE;
+  t_last_launches = 0;
+  if (!dw) return RMSN_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {
+    cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)hidden * sizeof(float), st);
+    return e == cudaSuccess ? RMSN_OK : cuda_fail(e);
+  }
+  if (!dy || !x || !gamma || !rstd || !dx || !workspace) return RMSN_ERR_NULL;
+  if (!aligned16(workspace)) return RMSN_ERR_ALIGN;
+  const size_t need = rms_norm_bwd_workspace_size(rows, hidden, dtype);
+  if (workspace_bytes < need) return RMSN_ERR_WORKSPACE;
+
+  const int s = elem_bytes(dtype);
+  BwdArgs a;
+  a.dy = dy;
+  a.x = x;
+  a.gamma = gamma;
+  a.rstd = rstd;
+  a.dx = dx;
+  a.dw = dw;
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.offset = offset;
+  a.vec_ok = ((hidden * s) % 16 == 0) && aligned16(dy) && aligned16(x) && aligned16(gamma) &&
+             aligned16(dx);
+  a.partial = static_cast<float*>(workspace);
+  a.max_partials = (int64_t)(workspace_bytes / ((size_t)hidden * sizeof(float)));
+  if (a.max_partials > RMSN_MAX_PARTIALS) a.max_partials = RMSN_MAX_PARTIALS;
+  int launches = 0;
+  cudaError_t e = launch_bwd(dtype, a, st, &launches);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = launches;
+  return RMSN_OK;
+}
+
+const char* rms_norm_status_string(int status) {
+  switch (status) {
+    case RMSN_OK: return "ok";
+    case RMSN_ERR_NULL: return "a required pointer is NULL";
+    case RMSN_ERR_SHAPE: return "rows or hidden out of range";
+    case RMSN_ERR_EPS: return "eps must be finite and >= 0";
+    case RMSN_ERR_DTYPE: return "unknown dtype";
+    case RMSN_ERR_ALIGN: return "workspace must be 16-byte aligned";
+    case RMSN_ERR_WORKSPACE: return "workspace smaller than rms_norm_bwd_workspace_size";
+    case RMSN_ERR_CUDA: return "a CUDA call failed";
+    case RMSN_ERR_ARG: return "offset must be 0 or 1 and cast_mode a rmsn_cast_mode";
+    default: return "unknown status";
+  }
+}
+
+int rms_norm_last_cuda_error(void) { return t_last_cuda_error; }
+
+int rms_norm_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,158 @@
+// Device helpers shared by the forward and backward kernels: 16-byte vector
+// loads/stores, conversion of packed storage types to fp32 and back, and the
+// fixed-order reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+// ---------------------------------------------------------------------------
+// storage types
+// ---------------------------------------------------------------------------
+template <typename T> struct Traits;
+template <> struct Traits<float> {
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+  __device__ static float to_f(float v) { return v; }
+  __device__ static float from_f(float v) { return v; }
+};
+template <> struct Traits<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+template <> struct Traits<__half> {
+  static constexpr int kVec = 8;
+  __device__ static float to_f(__half v) { return __half2float(v); }
+  __device__ static __half from_f(float v) { return __float2half_rn(v); }
+};
+
+// Round an fp32 value to T and back (the intermediate of the round-twice
+// store).
+template <typename T>
+__device__ __forceinline__ float round_trip(float v) {
+  return Traits<T>::to_f(Traits<T>::from_f(v));
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors
+// ---------------------------------------------------------------------------
+// Streaming read of data touched once per kernel (x, dy): bypass L1.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Read of data shared by every row (gamma): keep it in L1.
+__device__ __forceinline__ uint4 ld_shared_ro(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ void st_vec(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+               :
+               : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4& v, float (&f)[Traits<T>::kVec]);
+
+template <>
+__device__ __forceinline__ void unpack<float>(const uint4& v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+
+template <>
+__device__ __forceinline__ void unpack<__nv_bfloat16>(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <>
+__device__ __forceinline__ void unpack<__half>(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+    float2 t = __half22float2(h);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack(const float (&f)[Traits<T>::kVec]);
+
+template <>
+__device__ __forceinline__ uint4 pack<float>(const float (&f)[4]) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                    __float_as_uint(f[2]), __float_as_uint(f[3]));
+}
+
+template <>
+__device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <>
+__device__ __forceinline__ uint4 pack<__half>(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---------------------------------------------------------------------------
+// reductions (fixed order: the butterfly below gives every lane the same sum)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+
+// Sum of `v` over the whole CTA.  `red` holds 2 x 32 floats; `parity`
+// alternates between calls so that one __syncthreads per call suffices: a
+// thread can only overwrite slot p after every thread has passed the barrier
+// of the intervening call, i.e. after all reads of slot p are done.
+__device__ __forceinline__ float block_sum(float v, float* red, int parity) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  float* slot = red + 32 * parity;
+  if (lane == 0) slot[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int w = 0; w < nwarps; ++w) s += slot[w];
+  return s;
+}
+
+// Correctly rounded 1/sqrt(v).
+__device__ __forceinline__ float rstd_of(float mean_sq, float eps) {
+  return __frsqrt_rn(mean_sq + eps);
+}
+
+}  // namespace rmsn

@@ -1,0 +1,207 @@
+// RMSNorm forward kernels for sm_103a.
+//
+// Per row: fp32 sum of squares, rstd = 1/sqrt(sum/hidden + eps) stored in
+// fp32, then y = round(x * rstd * gain) with a single rounding (round once)
+// or y = round(round(x * rstd) * gain) (round twice) -- "Den dolda
+// avrundningen i RMSNorm", sections "En välbekant operation" and "Två
+// ställen att avrunda"; statistics in fp32 as in Liger-Kernel PR #92.
+//
+// The path is bound by HBM bandwidth: each element is read once and written
+// once, so the row stays in registers between the reduction and the store.
+// Three kernels:
+//   fwd_warp_rows  one warp per row (rows of at most 128 vectors),
+//   fwd_cta_row    one CTA per row (up to 1024 threads x 8 vectors),
+//   fwd_scalar     any alignment or width: scalar loads, the row is read a
+//                  second time for the store (from L1/L2).
+#include "common.cuh"
+#include "launch.h"
+
+namespace rmsn {
+namespace {
+
+// Output of one vector of x (already unpacked) for the chosen store.
+template <typename T>
+__device__ __forceinline__ uint4 scale_vec(const float (&xf)[Traits<T>::kVec],
+                                           const uint4& gv, float rs, float off,
+                                           int twice) {
+  constexpr int E = Traits<T>::kVec;
+  float gf[E], o[E];
+  unpack<T>(gv, gf);
+  if (twice) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) o[i] = round_trip<T>(xf[i] * rs) * (gf[i] + off);
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) o[i] = (xf[i] * rs) * (gf[i] + off);
+  }
+  return pack<T>(o);
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(256) fwd_warp_rows(
+    const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+    float* __restrict__ rstd, int64_t rows, int hidden, float eps, float off,
+    int twice) {
+  constexpr int E = Traits<T>::kVec;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;  // whole warps leave together
+  const int nvec = hidden / E;
+  const T* xr = x + row * hidden;
+  T* yr = y + row * hidden;
+
+  uint4 xv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + 32 * k;
+    xv[k] = v < nvec ? ld_stream(xr + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    float f[E];
+    unpack<T>(xv[k], f);
+#pragma unroll
+    for (int i = 0; i < E; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+  ss = warp_sum(ss);
+  const float rs = rstd_of(ss / (float)hidden, eps);
+  if (lane == 0) rstd[row] = rs;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = lane + 32 * k;
+    if (v < nvec) {
+      float f[E];
+      unpack<T>(xv[k], f);
+      const uint4 gv = ld_shared_ro(gamma + (int64_t)v * E);
+      st_vec(yr + (int64_t)v * E, scale_vec<T>(f, gv, rs, off, twice));
+    }
+  }
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) fwd_cta_row(
+    const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+    float* __restrict__ rstd, int hidden, float eps, float off, int twice) {
+  constexpr int E = Traits<T>::kVec;
+  __shared__ float red[64];
+  const int64_t row = blockIdx.x;
+  const int nvec = hidden / E;
+  const T* xr = x + row * hidden;
+  T* yr = y + row * hidden;
+
+  uint4 xv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = threadIdx.x + k * blockDim.x;
+    xv[k] = v < nvec ? ld_stream(xr + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    float f[E];
+    unpack<T>(xv[k], f);
+#pragma unroll
+    for (int i = 0; i < E; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+  ss = block_sum(ss, red, 0);
+  const float rs = rstd_of(ss / (float)hidden, eps);
+  if (threadIdx.x == 0) rstd[row] = rs;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = threadIdx.x + k * blockDim.x;
+    if (v < nvec) {
+      float f[E];
+      unpack<T>(xv[k], f);
+      const uint4 gv = ld_shared_ro(gamma + (int64_t)v * E);
+      st_vec(yr + (int64_t)v * E, scale_vec<T>(f, gv, rs, off, twice));
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) fwd_scalar(
+    const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+    float* __restrict__ rstd, int hidden, float eps, float off, int twice) {
+  __shared__ float red[64];
+  const int64_t row = blockIdx.x;
+  const T* xr = x + row * hidden;
+  T* yr = y + row * hidden;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < hidden; j += blockDim.x) {
+    const float f = Traits<T>::to_f(xr[j]);
+    ss = fmaf(f, f, ss);
+  }
+  ss = block_sum(ss, red, 0);
+  const float rs = rstd_of(ss / (float)hidden, eps);
+  if (threadIdx.x == 0) rstd[row] = rs;
+  for (int j = threadIdx.x; j < hidden; j += blockDim.x) {
+    const float xh = Traits<T>::to_f(xr[j]) * rs;
+    const float g = Traits<T>::to_f(gamma[j]) + off;
+    const float o = twice ? round_trip<T>(xh) * g : xh * g;
+    yr[j] = Traits<T>::from_f(o);
+  }
+}
+
+int pow2_at_least(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <typename T>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
+  constexpr int E = Traits<T>::kVec;
+  const T* x = static_cast<const T*>(a.x);
+  const T* g = static_cast<const T*>(a.gamma);
+  T* y = static_cast<T*>(a.y);
+  const float off = a.offset ? 1.f : 0.f;
+  const int nvec = a.hidden / E;
+
+  if (a.vec_ok && nvec <= 128) {
+    // one warp per row, 8 rows per CTA
+    const int vpt = pow2_at_least((nvec + 31) / 32);
+    const int64_t grid = (a.rows + 7) / 8;
+    switch (vpt) {
+      case 1: fwd_warp_rows<T, 1><<<(unsigned)grid, 256, 0, s>>>(x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      case 2: fwd_warp_rows<T, 2><<<(unsigned)grid, 256, 0, s>>>(x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      default: fwd_warp_rows<T, 4><<<(unsigned)grid, 256, 0, s>>>(x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+    }
+    *launches += 1;
+    return cudaGetLastError();
+  }
+  if (a.vec_ok) {
+    // one CTA per row; up to 4 vectors per thread at 1024 threads, 8 or 16
+    // at 512 threads (the register file holds the whole row)
+    int vpt = pow2_at_least((nvec + 255) / 256);
+    if (vpt > 16) vpt = 16;
+    const int tpr = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
+    if (tpr <= (vpt >= 8 ? 512 : 1024)) {
+      const unsigned grid = (unsigned)a.rows;
+      switch (vpt) {
+        case 1: fwd_cta_row<T, 1><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        case 2: fwd_cta_row<T, 2><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        case 4: fwd_cta_row<T, 4><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        case 8: fwd_cta_row<T, 8><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        default: fwd_cta_row<T, 16><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+      }
+      *launches += 1;
+      return cudaGetLastError();
+    }
+  }
+  fwd_scalar<T><<<(unsigned)a.rows, 256, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int dtype, const FwdArgs& a, cudaStream_t s, int* launches) {
+  switch (dtype) {
+    case 0: return launch_fwd_t<float>(a, s, launches);
+    case 1: return launch_fwd_t<__nv_bfloat16>(a, s, launches);
+    default: return launch_fwd_t<__half>(a, s, launches);
+  }
+}
+
+}  // namespace rmsn

@@ -1,0 +1,50 @@
+// Host-side launchers of the forward and backward kernels, called by the
+// C ABI in capi.cu after every argument has been validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+// Inputs of one forward call, already validated (rows >= 1).
+struct FwdArgs {
+  const void* x;
+  const void* gamma;
+  void* y;
+  float* rstd;
+  int64_t rows;
+  int hidden;
+  float eps;
+  int offset;      // 0: gain gamma, 1: gain 1 + gamma
+  int twice;       // 1: round x_hat to the storage type before the gain
+  bool vec_ok;     // 16-byte aligned rows: the vector kernels may run
+};
+
+// Inputs of one backward call, already validated (rows >= 1).
+struct BwdArgs {
+  const void* dy;
+  const void* x;
+  const void* gamma;
+  const float* rstd;
+  void* dx;
+  float* dw;
+  int64_t rows;
+  int hidden;
+  int offset;
+  bool vec_ok;
+  float* partial;          // fp32 workspace, >= max_partials * hidden floats
+  int64_t max_partials;    // partial rows the workspace holds
+};
+
+// dtype: 0 fp32, 1 bf16, 2 fp16.  Each returns the CUDA status of its
+// launches and adds the number of kernels it enqueued to *launches.
+cudaError_t launch_fwd(int dtype, const FwdArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_bwd(int dtype, const BwdArgs& a, cudaStream_t s, int* launches);
+
+// Device properties, cached per device.
+int sm_count(int device);
+int max_blocks_per_sm(const void* func, int block, size_t smem);
+
+}  // namespace rmsn

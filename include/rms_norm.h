@@ -1,0 +1,138 @@
+/*
+ * rms_norm.h -- C ABI of the GB300 fused RMSNorm forward/backward library
+ * (librms_norm_gb300.so).
+ *
+ * The operation.  For each row r of a row-major [rows, hidden] activation x:
+ *
+ *   rstd[r] = 1 / sqrt( (1/hidden) * sum_j x[r,j]^2 + eps )
+ *   x_hat   = x[r,j] * rstd[r]
+ *   y[r,j]  = x_hat * gain_j,   gain_j = gamma_j (offset 0) or 1 + gamma_j
+ *             (offset 1, the Gemma convention)
+ *
+ * as written in "Den dolda avrundningen i RMSNorm" (precisit.com), section
+ * "En välbekant operation" (the two displayed equations), with the Gemma
+ * gain of section "Vilken konvention hör till modellen?".  Statistics are
+ * accumulated in fp32 for every input type and the per-row rstd is stored in
+ * fp32 (Liger-Kernel PR #92 "feat: correct casts in RMSNorm to match
+ * references", the author's comment after the benchmark tables).
+ *
+ * The backward is the exact derivative of the forward (candle PR #4059 "Add
+ * backward passes to the fused rms_norm, layer_norm and softmax_last_dim
+ * ops" adds it with f32 statistics for half types but prints no formula):
+ *
+ *   g       = dy[r,j] * gain_j
+ *   c[r]    = (1/hidden) * sum_j g * x_hat
+ *   dx[r,j] = rstd[r] * (g - x_hat * c[r])
+ *   dw[j]   = sum_r dy[r,j] * x_hat      (fp32)
+ *
+ * Conventions common to every entry point:
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no device memory, keeps no per-call state and never
+ *    synchronises the stream.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream) of the current device; results are ready when the stream is.
+ *  - Layout: x, y, dy, dx are contiguous row-major [rows, hidden]; gamma and
+ *    dw are [hidden]; rstd is [rows].  x, gamma, y, dy, dx share `dtype`;
+ *    rstd, dw and the workspace are fp32.
+ *  - 128-bit vector kernels run when every [rows, hidden] and [hidden] pointer
+ *    is 16-byte aligned and hidden * element size is a multiple of 16; any
+ *    other alignment runs a scalar kernel with the same results.
+ *  - Every argument is checked on the host before anything is enqueued; on
+ *    an error nothing is enqueued and the status says why.  No C++ exception
+ *    crosses this interface.
+ */
+#ifndef RMS_NORM_GB300_H
+#define RMS_NORM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage type of x, gamma, y, dy and dx. */
+enum rmsn_dtype { RMSN_F32 = 0, RMSN_BF16 = 1, RMSN_F16 = 2 };
+
+/* Where the forward output is rounded ("Den dolda avrundningen i RMSNorm",
+ * section "Två ställen att avrunda"):
+ *   RMSN_ROUND_ONCE  -- y = round(x_hat * gain), the product taken in fp32;
+ *   RMSN_ROUND_TWICE -- y = round(round(x_hat) * gain), x_hat rounded to the
+ *                       storage type before the gain multiply (the Llama /
+ *                       MLX convention).
+ * Both round to nearest, ties to even.  For RMSN_F32 the two coincide. */
+enum rmsn_cast_mode { RMSN_ROUND_ONCE = 0, RMSN_ROUND_TWICE = 1 };
+
+enum rmsn_status {
+  RMSN_OK = 0,
+  RMSN_ERR_NULL = 1,       /* a required pointer is NULL */
+  RMSN_ERR_SHAPE = 2,      /* rows < 0, hidden < 1, hidden > RMSN_MAX_HIDDEN,
+                              or rows > RMSN_MAX_ROWS */
+  RMSN_ERR_EPS = 3,        /* eps negative, NaN or infinite */
+  RMSN_ERR_DTYPE = 4,      /* dtype not one of rmsn_dtype */
+  RMSN_ERR_ALIGN = 5,      /* workspace not 16-byte aligned */
+  RMSN_ERR_WORKSPACE = 6,  /* workspace smaller than rms_norm_bwd_workspace_size */
+  RMSN_ERR_CUDA = 7,       /* a CUDA call failed (see rms_norm_last_cuda_error) */
+  RMSN_ERR_ARG = 8         /* offset not 0/1 or cast_mode not a rmsn_cast_mode */
+};
+
+#define RMSN_MAX_HIDDEN 65536
+#define RMSN_MAX_ROWS 2147483647LL
+/* Upper bound on the number of fp32 weight-gradient partial rows the
+ * backward keeps in its workspace. */
+#define RMSN_MAX_PARTIALS 1024
+
+/*
+ * Forward.  Reads x [rows, hidden] and gamma [hidden]; writes y [rows,
+ * hidden] in `dtype` and rstd [rows] in fp32.  `eps` is added to the mean of
+ * squares under the root; it must be finite and >= 0.  `offset` 1 uses the
+ * gain 1 + gamma (formed in fp32).  `cast_mode` is a rmsn_cast_mode.
+ * rows == 0 enqueues nothing and returns RMSN_OK (x, y, rstd may then be
+ * NULL).  x and y must not overlap.
+ */
+int rms_norm_fwd(const void* x, const void* gamma, void* y, float* rstd,
+                 int64_t rows, int64_t hidden, float eps, int offset,
+                 int dtype, int cast_mode, void* stream);
+
+/*
+ * Bytes of fp32 workspace rms_norm_bwd needs for these sizes: room for
+ * min(rows, RMSN_MAX_PARTIALS) partial weight-gradient rows of `hidden`
+ * floats.  Depends only on its arguments (no device query).  Returns 0 for
+ * invalid arguments and for rows == 0.
+ */
+size_t rms_norm_bwd_workspace_size(int64_t rows, int64_t hidden, int dtype);
+
+/*
+ * Backward.  Reads dy, x [rows, hidden], gamma [hidden] and the fp32 rstd
+ * [rows] cached by the forward; writes dx [rows, hidden] in `dtype` and
+ * OVERWRITES dw [hidden] (fp32) with the weight gradient summed over all rows.
+ * The cast mode of the forward does not enter: the gradient is that of the
+ * unrounded forward.  `workspace` is caller-owned device scratch of at least
+ * rms_norm_bwd_workspace_size(rows, hidden, dtype) bytes, 16-byte aligned;
+ * its contents need no initialisation and are clobbered.  dw is reduced from
+ * per-block partials in a fixed order, so repeated calls with the same sizes
+ * on the same GPU model give bit-identical results.  rows == 0 zero-fills dw
+ * and returns RMSN_OK (dy, x, rstd, dx, workspace may then be NULL).
+ * Outputs must not overlap inputs.
+ */
+int rms_norm_bwd(const void* dy, const void* x, const void* gamma,
+                 const float* rstd, void* dx, float* dw,
+                 int64_t rows, int64_t hidden, int offset, int dtype,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* rms_norm_status_string(int status);
+
+/* The cudaError_t of the last call that returned RMSN_ERR_CUDA on this
+ * thread (0 if none). */
+int rms_norm_last_cuda_error(void);
+
+/* Number of kernels the last successful rms_norm_fwd / rms_norm_bwd call on
+ * this thread enqueued (0 when nothing was launched). */
+int rms_norm_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMS_NORM_GB300_H */

@@ -1,0 +1,115 @@
+"""Tolerance checks of GPU results against the oracle (test helper).
+
+The numbers come with the hot path's specification: fp32 outputs within a
+relative 1e-5, bf16/fp16 y and dx within one ulp of the output format with
+at least 99.9% of elements bit-identical, rstd within a relative 1e-6, dw
+within a relative 1e-3.  The readings of these numbers used here:
+
+* relative errors are taken against max(|ref|, s) where s is the rms over
+  the row of the terms the output is formed from: the ref row itself for y,
+  and rstd * g (g = dy * gain) for dx.  dx = rstd * (g - x_hat * c) can
+  cancel -- completely so for a one-element row, where it is
+  rstd * g * eps / (x**2 + eps) -- and fp32 arithmetic cannot resolve an
+  element far below the size of the terms it subtracts;
+* for half outputs the same floor applies -- an element passes with at most
+  one ulp OR with |got - ref| <= 1e-5 * s;
+* round twice rounds x_hat to the storage type, a decision the kernel takes
+  on its fp32 x_hat.  Where the exact x_hat lies so close to a rounding
+  midpoint that an fp32 x_hat (relative error well under 4e-6) may fall on
+  either side, the output built from either neighbour is correct;
+* rstd: |got - ref| <= 1e-6 * ref elementwise; dw: |got - ref| <= 1e-3 *
+  max(|ref_j|, rms(ref)).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import rounding
+
+REL_F32 = 1e-5
+REL_RSTD = 1e-6
+REL_DW = 1e-3
+MIN_BIT_IDENTICAL = 0.999
+FLOOR_REL = 1e-5
+MIDPOINT_WINDOW = 4e-6
+
+
+def _row_rms(ref: np.ndarray) -> np.ndarray:
+    r = np.sqrt(np.mean(np.square(ref, dtype=np.float64), axis=-1, keepdims=True))
+    return np.broadcast_to(r, ref.shape)
+
+
+def check_rows(got: np.ndarray, ref: np.ndarray, fmt: str, alt=None, what="y", terms=None):
+    """Compare a [rows, hidden] output.  ``alt`` (optional) is a list of
+    (mask, values) pairs of other correct results; ``terms`` (optional, same
+    shape) holds the terms the output is formed from, whose row rms sets the
+    floor (default: the reference itself).  Returns a dict of stats and
+    raises AssertionError with a description when the check fails."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    scale = _row_rms(ref if terms is None else np.asarray(terms, dtype=np.float64))
+    floor = FLOOR_REL * scale
+    diff = np.abs(got - ref)
+    if fmt == "f32":
+        ok = diff <= REL_F32 * np.maximum(np.abs(ref), scale)
+        same = float(np.mean(got == ref))
+        worst_ulp = None
+    else:
+        ulps = rounding.ulp_distance(got, ref, fmt)
+        ok = (ulps <= 1) | (diff <= floor)
+        if alt is not None:
+            for mask, vals in alt:
+                ok |= mask & (got == vals)
+        same = float(np.mean(ulps == 0))
+        worst_ulp = int(ulps.max()) if ulps.size else 0
+    bad = np.argwhere(~ok)
+    if bad.size:
+        i = tuple(bad[0])
+        raise AssertionError(
+            f"{what}: {bad.shape[0]} elements out of tolerance; first at {i}: "
+            f"got {got[i]!r} ref {ref[i]!r}")
+    if fmt != "f32":
+        assert same >= MIN_BIT_IDENTICAL, f"{what}: only {same:.5f} bit-identical"
+    return {"bit_identical": same, "max_ulp": worst_ulp}
+
+
+def check_rstd(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rel = np.abs(got - ref) / np.abs(ref)
+    worst = float(rel.max()) if rel.size else 0.0
+    assert worst <= REL_RSTD, f"rstd: worst relative error {worst:.3e}"
+    return {"rstd_max_rel": worst}
+
+
+def check_dw(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = np.maximum(np.abs(ref), np.sqrt(np.mean(ref * ref)))
+    rel = np.abs(got - ref) / scale
+    worst = float(rel.max()) if rel.size else 0.0
+    assert worst <= REL_DW, f"dw: worst relative error {worst:.3e}"
+    return {"dw_max_rel": worst}
+
+
+def spacing_exponent(v: np.ndarray, fmt: str) -> np.ndarray:
+    p, emin, _ = rounding.FORMATS[fmt]
+    _, e = np.frexp(v)
+    return np.maximum(e - 1, emin) - (p - 1)
+
+
+def round_twice_alternatives(x_hat: np.ndarray, gain: np.ndarray, fmt: str):
+    """(mask, lower, upper): where x_hat is within the fp32 window of a
+    rounding midpoint of ``fmt``, the stores built from the neighbour below
+    and above x_hat."""
+    q = spacing_exponent(x_hat, fmt)
+    scaled = np.ldexp(x_hat, -q)
+    lo = np.ldexp(np.floor(scaled), q)
+    hi = np.ldexp(np.ceil(scaled), q)
+    mid = (lo + hi) / 2.0
+    mask = np.abs(x_hat - mid) <= MIDPOINT_WINDOW * np.abs(x_hat)
+    y_lo = rounding.round_to(lo * gain, fmt)
+    y_hi = rounding.round_to(hi * gain, fmt)
+    return mask, y_lo, y_hi

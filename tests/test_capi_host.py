@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+the header declares, and rejects bad arguments before touching CUDA.
+No case here reaches a kernel launch, so none needs a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rms_norm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import bwd_rms_norm_gb300 as L
+    from bwd_rms_norm_gb300 import build
+    if not os.path.exists(L.LIB_PATH):
+        build.build()
+    return L.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rms_norm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("rms_norm_fwd", "rms_norm_bwd", "rms_norm_bwd_workspace_size",
+              "rms_norm_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_declares_every_export():
+    import bwd_rms_norm_gb300 as L
+    assert sorted(L.EXPORTED) == declared_functions()
+
+
+def test_header_constants_match_binding():
+    import bwd_rms_norm_gb300 as L
+    text = open(HEADER).read()
+    consts = dict(re.findall(r"(RMSN_\w+)\s*=\s*(\d+)", text))
+    consts.update(dict(re.findall(r"#define\s+(RMSN_\w+)\s+(\d+)", text)))
+    for name in ("RMSN_F32", "RMSN_BF16", "RMSN_F16", "RMSN_ROUND_ONCE", "RMSN_ROUND_TWICE",
+                 "RMSN_OK", "RMSN_MAX_HIDDEN", "RMSN_MAX_PARTIALS"):
+        assert int(consts[name]) == getattr(L, name), name
+
+
+NULL = None
+FAKE = ctypes.c_void_p(0x1000)   # never dereferenced: every case fails validation first
+
+
+def fwd(lib, x=FAKE, g=FAKE, y=FAKE, r=FAKE, rows=4, hidden=64, eps=1e-5, offset=0,
+        dtype=1, mode=0):
+    return lib.rms_norm_fwd(x, g, y, r, rows, hidden, eps, offset, dtype, mode, None)
+
+
+def test_fwd_validation(lib):
+    assert fwd(lib, dtype=3) == 4
+    assert fwd(lib, dtype=-1) == 4
+    assert fwd(lib, offset=2) == 8
+    assert fwd(lib, mode=2) == 8
+    assert fwd(lib, rows=-1) == 2
+    assert fwd(lib, hidden=0) == 2
+    assert fwd(lib, hidden=65537) == 2
+    assert fwd(lib, rows=1 << 31) == 2
+    assert fwd(lib, eps=-1e-6) == 3
+    assert fwd(lib, eps=float("nan")) == 3
+    assert fwd(lib, eps=float("inf")) == 3
+    assert fwd(lib, x=NULL) == 1
+    assert fwd(lib, g=NULL) == 1
+    assert fwd(lib, y=NULL) == 1
+    assert fwd(lib, r=NULL) == 1
+    # zero rows: nothing to do, no pointer needed, nothing launched
+    assert fwd(lib, x=NULL, y=NULL, r=NULL, g=NULL, rows=0) == 0
+    assert lib.rms_norm_last_launch_count() == 0
+
+
+def bwd(lib, dy=FAKE, x=FAKE, g=FAKE, r=FAKE, dx=FAKE, dw=FAKE, rows=4, hidden=64, offset=0,
+        dtype=1, ws=FAKE, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.rms_norm_bwd_workspace_size(rows, hidden, dtype)
+    return lib.rms_norm_bwd(dy, x, g, r, dx, dw, rows, hidden, offset, dtype, ws, ws_bytes, None)
+
+
+def test_bwd_validation(lib):
+    assert bwd(lib, dtype=7) == 4
+    assert bwd(lib, offset=-1) == 8
+    assert bwd(lib, rows=-2) == 2
+    assert bwd(lib, hidden=70000) == 2
+    assert bwd(lib, dw=NULL) == 1
+    for k in ("dy", "x", "g", "r", "dx", "ws"):
+        assert bwd(lib, **{k: NULL}) == 1, k
+    assert bwd(lib, ws=ctypes.c_void_p(0x1004)) == 5
+    assert bwd(lib, ws_bytes=lib.rms_norm_bwd_workspace_size(4, 64, 1) - 4) == 6
+
+
+def test_workspace_size(lib):
+    assert lib.rms_norm_bwd_workspace_size(0, 64, 1) == 0
+    assert lib.rms_norm_bwd_workspace_size(10, 64, 1) == 10 * 64 * 4
+    assert lib.rms_norm_bwd_workspace_size(5000, 4096, 1) == 1024 * 4096 * 4
+    assert lib.rms_norm_bwd_workspace_size(5, 0, 1) == 0
+    assert lib.rms_norm_bwd_workspace_size(5, 64, 9) == 0
+
+
+def test_status_strings(lib):
+    for s in range(9):
+        assert lib.rms_norm_status_string(s).decode()
+    assert lib.rms_norm_status_string(99).decode() == "unknown status"
+
+
+def test_binding_refuses_cpu_tensors():
+    """The Python layer has no CPU path: CPU tensors are an error."""
+    import torch
+    import bwd_rms_norm_gb300 as L
+    x = torch.zeros(2, 8)
+    with pytest.raises(RuntimeError, match="CUDA"):
+        L.rms_norm_fwd(x, torch.ones(8), 1e-5)
