@@ -42,6 +42,7 @@ EXPORTED = (
     "rms_norm_status_string",
     "rms_norm_last_cuda_error",
     "rms_norm_last_launch_count",
+    "rms_norm_bwd_noalloc",
 )
 
 
@@ -78,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_last_cuda_error.restype = I
     lib.rms_norm_last_launch_count.argtypes = []
     lib.rms_norm_last_launch_count.restype = I
+    lib.rms_norm_bwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I, I, P]
+    lib.rms_norm_bwd_noalloc.restype = I
     _lib = lib
     return lib
 
@@ -188,4 +191,32 @@ def rms_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: t
                               _stream_handle(x.device, stream))
     if st != RMSN_OK:
         raise RMSNormError("rms_norm_bwd", st)
+    return dx, dw
+
+
+def rms_norm_bwd_noalloc(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor,
+                         rstd: torch.Tensor, offset: int = 0, dx: Optional[torch.Tensor] = None,
+                         dw: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None):
+    """Backward for callers that cannot allocate device scratch: the library
+    keeps the weight-gradient partials in its own fixed 16 MiB device array
+    (sizes needing more are refused).  Pass ``dx`` and ``dw`` to avoid any
+    allocation on the Python side as well.  Calls that may overlap on the GPU
+    share that array and must be ordered on one stream."""
+    lib = load_library()
+    for name, t in (("dy", dy), ("x", x), ("gamma", gamma), ("rstd", rstd)):
+        _check_cuda(name, t)
+    if dy.dtype != x.dtype or gamma.dtype != x.dtype or rstd.dtype != torch.float32:
+        raise RuntimeError("dy, x, gamma share one dtype; rstd is float32")
+    rows, hidden = _as_rows(x)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        st = lib.rms_norm_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx),
+                                      _ptr(dw), rows, hidden, int(offset), DTYPE_CODES[x.dtype],
+                                      _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_bwd_noalloc", st)
     return dx, dw

@@ -131,6 +131,36 @@ int rms_norm_last_cuda_error(void);
  * this thread enqueued (0 when nothing was launched). */
 int rms_norm_last_launch_count(void);
 
+/*
+ * Backward without caller-provided scratch.  The method's pages describe no
+ * such call; it exists for callers that cannot allocate device memory at the
+ * point where they run the backward -- for example a plugin whose enqueue
+ * hook must not call cudaMalloc, or a service that works inside a fixed,
+ * pre-reserved memory budget -- and so cannot supply the `workspace` that
+ * rms_norm_bwd asks for.
+ *
+ * Same arguments, results and errors as rms_norm_bwd minus the workspace.
+ * The per-block weight-gradient partials go to one fixed array of
+ * RMSN_NOALLOC_SCRATCH_BYTES (16 MiB) that the library declares in device
+ * memory; every GPU that loads the library holds it until the process exits.
+ * Sizes whose rms_norm_bwd_workspace_size exceeds RMSN_NOALLOC_SCRATCH_BYTES
+ * are rejected with RMSN_ERR_SHAPE before anything is enqueued.  This entry
+ * point calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The first call on each device looks up that device's address of the array
+ * (with the device current); make that first call before any stream capture.
+ * Every call on a device uses the same array and leaves its partials there;
+ * no part of it needs clearing, because every partial the reduction reads is
+ * written earlier in the same call.  Calls that may run at the same time on
+ * the GPU (different streams without ordering) race on the array and give
+ * wrong results: order them on one stream or with events.
+ */
+#define RMSN_NOALLOC_SCRATCH_BYTES (16u << 20)
+int rms_norm_bwd_noalloc(const void* dy, const void* x, const void* gamma,
+                         const float* rstd, void* dx, float* dw,
+                         int64_t rows, int64_t hidden, int offset, int dtype,
+                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif
