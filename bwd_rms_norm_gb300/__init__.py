@@ -43,6 +43,7 @@ EXPORTED = (
     "rms_norm_last_cuda_error",
     "rms_norm_last_launch_count",
     "rms_norm_bwd_noalloc",
+    "rms_norm_wait_timeouts",
 )
 
 
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_last_launch_count.restype = I
     lib.rms_norm_bwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I, I, P]
     lib.rms_norm_bwd_noalloc.restype = I
+    lib.rms_norm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.rms_norm_wait_timeouts.restype = I
     _lib = lib
     return lib
 
@@ -99,6 +102,16 @@ def rms_norm_bwd_workspace_size(rows: int, hidden: int, dtype) -> int:
 def last_launch_count() -> int:
     """Kernels enqueued by the last successful call on this thread."""
     return int(load_library().rms_norm_last_launch_count())
+
+
+def wait_timeouts() -> int:
+    """Bounded device waits that ran out since the library was loaded (0 in
+    correct operation); synchronises with the device."""
+    n = ctypes.c_uint(0)
+    st = load_library().rms_norm_wait_timeouts(ctypes.byref(n))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_wait_timeouts", st)
+    return int(n.value)
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:

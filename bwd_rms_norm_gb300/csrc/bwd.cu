@@ -189,28 +189,29 @@ __global__ void __launch_bounds__(256) bwd_scalar(
   }
 }
 
-// dw[j] = sum_b partial[b][j].  Block (32 columns) x (16 lanes over b): lane
-// t sums b = t, t+16, ... in increasing order, then lane 0 adds the 16 lane
+// dw[j] = sum_b partial[b][j].  Block (32 columns) x (32 lanes over b): lane
+// t sums b = t, t+32, ... in increasing order, then lane 0 adds the 32 lane
 // sums in order.  The order depends only on nparts.
-__global__ void __launch_bounds__(512) dw_finalize(const float* __restrict__ partial,
-                                                   float* __restrict__ dw, int nparts,
-                                                   int hidden) {
+__global__ void __launch_bounds__(1024) dw_finalize(const float* __restrict__ partial,
+                                                    float* __restrict__ dw, int nparts,
+                                                    int hidden) {
 #if __CUDA_ARCH__ >= 900
   cudaGridDependencySynchronize();
 #endif
-  __shared__ float s[16][33];
+  __shared__ float s[32][33];
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int j = blockIdx.x * 32 + tx;
   float a = 0.f;
   if (j < hidden) {
-    for (int b = ty; b < nparts; b += 16) a += partial[(int64_t)b * hidden + j];
+#pragma unroll 4
+    for (int b = ty; b < nparts; b += 32) a += partial[(int64_t)b * hidden + j];
   }
   s[ty][tx] = a;
   __syncthreads();
   if (ty == 0 && j < hidden) {
     float t = 0.f;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) t += s[q][tx];
+    for (int q = 0; q < 32; ++q) t += s[q][tx];
     dw[j] = t;
   }
 }
@@ -219,7 +220,7 @@ cudaError_t launch_finalize(const float* partial, float* dw, int nparts, int hid
                             cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((hidden + 31) / 32));
-  cfg.blockDim = dim3(32, 16);
+  cfg.blockDim = dim3(32, 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -248,6 +249,11 @@ cudaError_t launch_rows(const BwdArgs& a, int tpr, cudaStream_t s, int* nparts) 
   return cudaGetLastError();
 }
 
+template <typename T> int dtype_code();
+template <> int dtype_code<float>() { return 0; }
+template <> int dtype_code<__nv_bfloat16>() { return 1; }
+template <> int dtype_code<__half>() { return 2; }
+
 template <typename T>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s, int* launches) {
   constexpr int E = Traits<T>::kVec;
@@ -255,8 +261,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s, int* launches) {
   const int max_vpt = E == 4 ? 4 : 2;  // at most 16 columns per thread
   int nparts = 0;
   cudaError_t e = cudaErrorInvalidValue;
-  bool done = false;
-  if (a.vec_ok) {
+  // the staged pipeline where x and dy rows fit its ring, else the register
+  // kernel, else (rows too wide for one CTA) a thread-block cluster, else the
+  // scalar kernel
+  bool done = try_launch_bwd_tma(dtype_code<T>(), a, s, &e, &nparts);
+  if (!done && a.vec_ok) {
     int vpt = 1;
     while (vpt < max_vpt && (nvec + vpt - 1) / vpt > 1024) vpt <<= 1;
     const int tpr = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
@@ -267,6 +276,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s, int* launches) {
       done = true;
     }
   }
+  if (!done) done = try_launch_bwd_cluster(dtype_code<T>(), a, s, &e, &nparts);
   if (!done) {
     int dev = 0;
     e = cudaGetDevice(&dev);

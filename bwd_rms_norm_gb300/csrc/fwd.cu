@@ -143,6 +143,11 @@ __global__ void __launch_bounds__(256) fwd_scalar(
   }
 }
 
+template <typename T> int dtype_code();
+template <> int dtype_code<float>() { return 0; }
+template <> int dtype_code<__nv_bfloat16>() { return 1; }
+template <> int dtype_code<__half>() { return 2; }
+
 int pow2_at_least(int v) {
   int p = 1;
   while (p < v) p <<= 1;
@@ -189,6 +194,11 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
       return cudaGetLastError();
     }
   }
+  cudaError_t e = cudaSuccess;
+  if (try_launch_fwd_cluster(dtype_code<T>(), a, s, &e)) {
+    if (e == cudaSuccess) *launches += 1;
+    return e;
+  }
   fwd_scalar<T><<<(unsigned)a.rows, 256, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice);
   *launches += 1;
   return cudaGetLastError();
@@ -196,7 +206,18 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
 
 }  // namespace
 
+// Kernel choice by row width (measured on GB300 with the workloads of the
+// tests): rows of up to 16 KB run the register kernels (a row per CTA, 8
+// CTAs per SM in flight); wider rows run the staged TMA pipeline where its
+// ring and registers hold them, else the register kernels, and rows too wide
+// for those are split over a thread-block cluster.
 cudaError_t launch_fwd(int dtype, const FwdArgs& a, cudaStream_t s, int* launches) {
+  cudaError_t e = cudaSuccess;
+  const int row_bytes = a.hidden * (dtype == 0 ? 4 : 2);
+  if (row_bytes > 16 * 1024 && try_launch_fwd_tma(dtype, a, s, &e)) {
+    if (e == cudaSuccess) *launches += 1;
+    return e;
+  }
   switch (dtype) {
     case 0: return launch_fwd_t<float>(a, s, launches);
     case 1: return launch_fwd_t<__nv_bfloat16>(a, s, launches);

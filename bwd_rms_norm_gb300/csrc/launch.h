@@ -43,6 +43,18 @@ struct BwdArgs {
 cudaError_t launch_fwd(int dtype, const FwdArgs& a, cudaStream_t s, int* launches);
 cudaError_t launch_bwd(int dtype, const BwdArgs& a, cudaStream_t s, int* launches);
 
+// TMA-staged persistent kernels (tma.cu).  Each returns false, having
+// enqueued nothing, when the sizes or alignment do not suit it; otherwise
+// true with the launch status in *err (and the partial count in *nparts).
+bool try_launch_fwd_tma(int dtype, const FwdArgs& a, cudaStream_t s, cudaError_t* err);
+bool try_launch_bwd_tma(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
+                        int* nparts);
+
+// Cluster kernels for wide rows (cluster.cu), same contract.
+bool try_launch_fwd_cluster(int dtype, const FwdArgs& a, cudaStream_t s, cudaError_t* err);
+bool try_launch_bwd_cluster(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
+                            int* nparts);
+
 // Device properties, cached per device.
 int sm_count(int device);
 int max_blocks_per_sm(const void* func, int block, size_t smem);

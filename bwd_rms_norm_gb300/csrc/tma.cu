@@ -1,0 +1,628 @@
+// Persistent, TMA-staged, warp-specialised forward and backward kernels for
+// sm_103a.
+//
+// The path is bound by HBM bandwidth.  A row-wise normalisation cannot
+// write any output of a row before the whole row has been reduced, so two
+// things decide the speed: how many bytes each SM keeps in flight, and that
+// the latency of each row's reduction never stalls the stream of outputs.
+// One CTA per SM owns a contiguous range of rows and splits its warps into
+// three roles that meet at per-stage mbarriers:
+//
+//   producer (warp 0, one thread)  streams the CTA's rows into a ring of
+//       shared-memory stages with 1D bulk copies (cp.async.bulk, the TMA
+//       engine) -- 8 to 32 stages, i.e. 100-200 KB of reads in flight per SM
+//       without any of it held in registers;                     -> full[s]
+//   reducers (warps 1..R)  one warp per row (warp d takes the CTA's rows
+//       d, d + R, ...): the row statistic -- rstd in the forward,
+//       c = sum(g * x_hat) / hidden in the backward -- into the stage's slot;
+//                                                                 -> red[s]
+//   appliers (the remaining threads)  walk every row in order; each thread
+//       owns the same 16-byte vectors of every row, keeps their fp32 gains
+//       (and in the backward their fp32 dw accumulators) in registers, and
+//       writes y or dx with 128-bit stores.  No barrier among the appliers.
+//
+// A stage is released (empty[s]) when its reducer and every applier warp
+// have read it.  The stage count is a multiple of R, so reducer d only ever
+// uses the stages s = d (mod R) and sees every phase of their barriers in
+// order, like the producer and the appliers, which walk all stages in order:
+// an mbarrier parity wait is only unambiguous for a waiter that has seen the
+// phase before it.  Numerics are those of the register kernels: fp32 sums of
+// squares and dots, rstd = 1/sqrt(mean + eps) correctly rounded, one rounding
+// at the store (two for the round-twice forward).
+//
+// Every wait on an mbarrier is bounded (about one second of %globaltimer).
+// A wait that runs out counts in a device error counter, raises an abort
+// flag in shared memory so that every other wait of the CTA returns at once,
+// and the CTA drains: the producer waits (again bounded) for each bulk copy
+// it issued before it exits.  rms_norm_wait_timeouts() reports the count.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+#include "rms_norm.h"
+
+namespace rmsn {
+
+namespace {
+
+__device__ unsigned int g_wait_timeouts;
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // ~1 s
+constexpr int kMaxStages = 32;
+constexpr int kMaxThreads = 1024;
+constexpr int kMaxReducers = 12;
+// Dynamic shared memory for the ring (and the backward's fp32 gain row).
+constexpr int kRingBudget = 200 * 1024;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// 1D bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Wait for phase `parity` of `bar`.  Returns false if the CTA is aborting or
+// the wait ran out (which starts the abort).
+__device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      atomicAdd(&g_wait_timeouts, 1u);
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used to drain copies in flight.
+__device__ void drain_phase(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) {
+      atomicAdd(&g_wait_timeouts, 1u);
+      return;
+    }
+  }
+}
+
+// Barriers and per-stage values of the pipeline (static shared memory).
+struct Pipe {
+  uint64_t full[kMaxStages];   // the stage's bulk copies landed
+  uint64_t red[kMaxStages];    // a reducer wrote stat[s]
+  uint64_t empty[kMaxStages];  // reducer and appliers are done with the stage
+  float stat[kMaxStages];      // rstd (forward) or c (backward) of the stage's row
+  int abort;
+};
+
+// The rows a CTA owns: the contiguous range [r0, r0 + n) of an even split
+// of all rows over the grid.
+struct Rows {
+  int64_t r0;
+  int n;
+  __device__ __forceinline__ int64_t row(int i) const { return r0 + i; }
+};
+
+__device__ __forceinline__ Rows cta_rows(int64_t rows) {
+  Rows r;
+  r.r0 = (int64_t)blockIdx.x * rows / gridDim.x;
+  r.n = (int)((int64_t)(blockIdx.x + 1) * rows / gridDim.x - r.r0);
+  return r;
+}
+
+// Position in the ring: stage index and phase parity, advanced without
+// division.
+struct RingPos {
+  int stage;
+  uint32_t phase;
+  __device__ __forceinline__ void advance(int by, int stages) {
+    stage += by;
+    while (stage >= stages) {
+      stage -= stages;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Called by every thread; thread s initialises stage s's barriers.  The
+// caller synchronises the CTA afterwards.
+__device__ __forceinline__ void init_pipe(Pipe& p, int stages, int applier_warps) {
+  const int s = threadIdx.x;
+  if (s == 0) p.abort = 0;
+  if (s < stages) {
+    mbar_init(&p.full[s], 1);
+    mbar_init(&p.red[s], 1);
+    mbar_init(&p.empty[s], 1 + applier_warps);
+    fence_mbar_init();
+  }
+}
+
+// Producer: issue the copies of the CTA's rows (its i-th row is rw.row(i))
+// into the ring.  NSRC source tensors go to consecutive parts of a stage.
+template <int NSRC>
+__device__ void produce(Pipe& p, unsigned char* ring, int stride, int stages,
+                        const void* const (&src)[NSRC], const Rows& rw, uint32_t row_bytes,
+                        volatile int* abort) {
+  RingPos pos{0, 0u};
+  int i = 0;
+  const int n = rw.n;
+  for (; i < n; ++i) {
+    // the stage's previous use (parity phase ^ 1) must be released first
+    if (i >= stages && !wait_phase(&p.empty[pos.stage], pos.phase ^ 1u, abort)) break;
+    unsigned char* dst = ring + (size_t)pos.stage * stride;
+    mbar_arrive_expect_tx(&p.full[pos.stage], NSRC * row_bytes);
+    const size_t off = (size_t)rw.row(i) * row_bytes;
+#pragma unroll
+    for (int t = 0; t < NSRC; ++t)
+      bulk_load(dst + t * row_bytes, static_cast<const unsigned char*>(src[t]) + off, row_bytes,
+                &p.full[pos.stage]);
+    pos.advance(1, stages);
+  }
+  // Before the CTA may exit every copy issued must have landed: the last
+  // min(i, stages) issues are the latest use of each stage; walk back.
+  const int outstanding = i < stages ? i : stages;
+  for (int q = 0; q < outstanding; ++q) {
+    if (pos.stage == 0) {
+      pos.stage = stages - 1;
+      pos.phase ^= 1u;
+    } else {
+      --pos.stage;
+    }
+    drain_phase(&p.full[pos.stage], pos.phase);
+  }
+}
+
+// Sum of per-element partial sums, pairwise.
+template <int E>
+__device__ __forceinline__ float pairwise(float (&p)[E]) {
+#pragma unroll
+  for (int w = E / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int e = 0; e < w; ++e) p[e] += p[e + w];
+  return p[0];
+}
+
+// Forward.  Reducer: sum of squares of its row, rstd, written to global and
+// to the stage's slot.  Appliers: y = round((x * rstd) * gain) (or the
+// round-twice store) for their vectors of every row.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
+    const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+    float* __restrict__ rstd, int64_t rows, int hidden, float eps, float off, int twice,
+    int stages, int reducers) {
+  constexpr int E = Traits<T>::kVec;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Pipe pipe;
+  const int row_bytes = hidden * (int)sizeof(T);
+  const int stride = (row_bytes + 127) / 128 * 128;
+  const int appliers = blockDim.x - 32 * (1 + reducers);
+  const Rows rw = cta_rows(rows);
+  const int n = rw.n;
+  init_pipe(pipe, stages, appliers / 32);
+  __syncthreads();
+  volatile int* abort = &pipe.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = hidden / E;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const void* const src[1] = {x};
+      produce<1>(pipe, smem, stride, stages, src, rw, (uint32_t)row_bytes, abort);
+    }
+    return;
+  }
+
+  if (warp <= reducers) {
+    const int d = warp - 1;
+    RingPos pos{0, 0u};
+    pos.advance(d, stages);
+    for (int i = d; i < n; i += reducers) {
+      // a warp leaves as a whole: a wait that failed on any lane ends it
+      if (!__all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort))) return;
+      const uint4* st = reinterpret_cast<const uint4*>(smem + (size_t)pos.stage * stride);
+      float part[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) part[e] = 0.f;
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
+        float f[E];
+        unpack<T>(st[v], f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[e] = fmaf(f[e], f[e], part[e]);
+      }
+      const float ss = warp_sum(pairwise<E>(part));
+      const float rs = rstd_of(ss / (float)hidden, eps);
+      if (lane == 0) {
+        rstd[rw.row(i)] = rs;
+        pipe.stat[pos.stage] = rs;
+        mbar_arrive(&pipe.red[pos.stage]);
+        mbar_arrive(&pipe.empty[pos.stage]);
+      }
+      pos.advance(reducers, stages);
+    }
+    return;
+  }
+
+  const int a = threadIdx.x - 32 * (1 + reducers);
+  float ge[VPT][E];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = a + j * appliers;
+    const uint4 g4 = v < nvec ? ld_shared_ro(gamma + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+    unpack<T>(g4, ge[j]);
+#pragma unroll
+    for (int e = 0; e < E; ++e) ge[j][e] += off;
+  }
+  RingPos pos{0, 0u};
+  for (int i = 0; i < n; ++i) {
+    bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
+    ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const float rs = pipe.stat[pos.stage];
+    const uint4* st = reinterpret_cast<const uint4*>(smem + (size_t)pos.stage * stride);
+    T* yr = y + rw.row(i) * hidden;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = a + j * appliers;
+      if (v < nvec) {
+        float f[E], o[E];
+        unpack<T>(st[v], f);
+        if (twice) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[e] = round_trip<T>(f[e] * rs) * ge[j][e];
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[e] = (f[e] * rs) * ge[j][e];
+        }
+        st_vec(yr + (int64_t)v * E, pack<T>(o));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
+    pos.advance(1, stages);
+  }
+}
+
+// Backward.  Reducer: c = sum(dy * gain * x * rstd) / hidden of its row,
+// reading the fp32 gains from a shared-memory copy.  Appliers: dx =
+// rstd * (dy * gain - x_hat * c) for their vectors of every row, and the
+// fp32 dw accumulators of those columns, written once at the end as the
+// CTA's partial row.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
+    const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
+    const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
+    int64_t rows, int hidden, float off, int stages, int reducers) {
+  constexpr int E = Traits<T>::kVec;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Pipe pipe;
+#if __CUDA_ARCH__ >= 900
+  // Let the finalize kernel be scheduled now; it waits for this grid to
+  // complete before reading the partials.
+  cudaTriggerProgrammaticLaunchCompletion();
+#endif
+  const int row_bytes = hidden * (int)sizeof(T);
+  const int stride = (2 * row_bytes + 127) / 128 * 128;
+  const int gain_bytes = (hidden * 4 + 127) / 128 * 128;
+  float* gain = reinterpret_cast<float*>(smem);
+  unsigned char* ring = smem + gain_bytes;
+  const int appliers = blockDim.x - 32 * (1 + reducers);
+  const Rows rw = cta_rows(rows);
+  const int n = rw.n;
+  init_pipe(pipe, stages, appliers / 32);
+  __syncthreads();
+  volatile int* abort = &pipe.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = hidden / E;
+  const int doff = row_bytes / 16;  // dy part of a stage, in 16-byte vectors
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const void* const src[2] = {x, dy};
+      produce<2>(pipe, ring, stride, stages, src, rw, (uint32_t)row_bytes, abort);
+    }
+    return;
+  }
+
+  if (warp <= reducers) {
+    // the reducers stage the fp32 gains while the first copies are in flight
+    for (int j = threadIdx.x - 32; j < hidden; j += 32 * reducers)
+      gain[j] = Traits<T>::to_f(gamma[j]) + off;
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * reducers) : "memory");
+    const float4* g4 = reinterpret_cast<const float4*>(gain);
+    const int d = warp - 1;
+    RingPos pos{0, 0u};
+    pos.advance(d, stages);
+    for (int i = d; i < n; i += reducers) {
+      const float rs = __ldg(rstd + rw.row(i));
+      if (!__all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort))) return;
+      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+      float part[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) part[e] = 0.f;
+#pragma unroll 2
+      for (int v = lane; v < nvec; v += 32) {
+        float xf[E], df[E], gf[E];
+        unpack<T>(st[v], xf);
+        unpack<T>(st[doff + v], df);
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+          const float4 q = g4[(v * E + e) / 4];
+          gf[e] = q.x;
+          gf[e + 1] = q.y;
+          gf[e + 2] = q.z;
+          gf[e + 3] = q.w;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[e] = fmaf(df[e] * gf[e], xf[e] * rs, part[e]);
+      }
+      const float dot = warp_sum(pairwise<E>(part));
+      if (lane == 0) {
+        pipe.stat[pos.stage] = dot / (float)hidden;
+        mbar_arrive(&pipe.red[pos.stage]);
+        mbar_arrive(&pipe.empty[pos.stage]);
+      }
+      pos.advance(reducers, stages);
+    }
+    return;
+  }
+
+  const int a = threadIdx.x - 32 * (1 + reducers);
+  float ge[VPT][E], acc[VPT][E];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = a + j * appliers;
+    const uint4 q = v < nvec ? ld_shared_ro(gamma + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+    unpack<T>(q, ge[j]);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      ge[j][e] += off;
+      acc[j][e] = 0.f;
+    }
+  }
+  RingPos pos{0, 0u};
+  float rs_next = n > 0 ? __ldg(rstd + rw.row(0)) : 0.f;
+  for (int i = 0; i < n; ++i) {
+    const float rs = rs_next;
+    if (i + 1 < n) rs_next = __ldg(rstd + rw.row(i + 1));
+    bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
+    ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const float c = pipe.stat[pos.stage];
+    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+    T* dxr = dx + rw.row(i) * hidden;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = a + j * appliers;
+      if (v < nvec) {
+        float xf[E], df[E], o[E];
+        unpack<T>(st[v], xf);
+        unpack<T>(st[doff + v], df);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float xh = xf[e] * rs;
+          acc[j][e] = fmaf(df[e], xh, acc[j][e]);
+          o[e] = fmaf(-xh, c, df[e] * ge[j][e]) * rs;
+        }
+        st_vec(dxr + (int64_t)v * E, pack<T>(o));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
+    pos.advance(1, stages);
+  }
+  float* pr = partial + (int64_t)blockIdx.x * hidden;
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = a + j * appliers;
+    if (v < nvec) {
+#pragma unroll
+      for (int e = 0; e < E; e += 4)
+        *reinterpret_cast<float4*>(pr + (int64_t)v * E + e) =
+            make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
+    }
+  }
+}
+
+std::mutex g_attr_mutex;
+struct AttrEntry {
+  const void* func;
+  int device;
+};
+AttrEntry g_attr_done[128];
+int g_attr_n = 0;
+
+// Raise a kernel's dynamic shared memory limit, once per (kernel, device).
+cudaError_t allow_smem(const void* kern) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  for (int i = 0; i < g_attr_n; ++i)
+    if (g_attr_done[i].func == kern && g_attr_done[i].device == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBudget);
+  if (e == cudaSuccess && g_attr_n < 128) g_attr_done[g_attr_n++] = AttrEntry{kern, dev};
+  return e;
+}
+
+// Applier threads: the fewest vectors per thread that keep them within
+// `max_a` threads, at most `max_vpt`.  Returns 0 when no split fits.
+int pick_vpt(int nvec, int max_a, int max_vpt, int* appliers) {
+  int vpt = 1;
+  while (vpt < max_vpt && (nvec + vpt - 1) / vpt > max_a) vpt <<= 1;
+  const int a = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
+  if (a > max_a) return 0;
+  *appliers = a;
+  return vpt;
+}
+
+// Stage and reducer counts from the number of stages that fit: every
+// reducer owns the same number of stages (see the note at the top).
+void split_stages(int fit, int* stages, int* reducers) {
+  if (fit > kMaxStages) fit = kMaxStages;
+  if (fit <= kMaxReducers) {
+    *stages = fit;
+    *reducers = fit;
+  } else {
+    *reducers = 8;
+    *stages = fit / 8 * 8;
+  }
+}
+
+int grid_for(int64_t rows, int64_t cap, cudaError_t* err) {
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+  int64_t g = sm_count(dev);
+  if (g > rows) g = rows;
+  if (g > cap) g = cap;
+  return (int)g;
+}
+
+template <typename T, int VPT>
+cudaError_t launch_fwd_tma_v(const FwdArgs& a, int appliers, int stages, int reducers, int grid,
+                             cudaStream_t s) {
+  auto kern = fwd_tma<T, VPT>;
+  const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  cudaError_t e = allow_smem((const void*)kern);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 32 * (1 + reducers) + appliers, stages * stride, s>>>(
+      static_cast<const T*>(a.x), static_cast<const T*>(a.gamma), static_cast<T*>(a.y), a.rstd,
+      a.rows, a.hidden, a.eps, a.offset ? 1.f : 0.f, a.twice, stages, reducers);
+  return cudaGetLastError();
+}
+
+template <typename T>
+bool try_fwd_tma_t(const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
+  constexpr int E = Traits<T>::kVec;
+  const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  int stages = 0, reducers = 0;
+  split_stages(kRingBudget / stride, &stages, &reducers);
+  if (stages < 3) return false;
+  int appliers = 0;
+  // at most 4 vectors per applier (gains in fp32 registers)
+  const int vpt = pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 4, &appliers);
+  if (vpt == 0) return false;
+  const int grid = grid_for(a.rows, a.rows, err);
+  if (*err != cudaSuccess) return true;
+  switch (vpt) {
+    case 1: *err = launch_fwd_tma_v<T, 1>(a, appliers, stages, reducers, grid, s); break;
+    case 2: *err = launch_fwd_tma_v<T, 2>(a, appliers, stages, reducers, grid, s); break;
+    default: *err = launch_fwd_tma_v<T, 4>(a, appliers, stages, reducers, grid, s); break;
+  }
+  return true;
+}
+
+template <typename T, int VPT>
+cudaError_t launch_bwd_tma_v(const BwdArgs& a, int appliers, int stages, int reducers, int grid,
+                             cudaStream_t s) {
+  auto kern = bwd_tma<T, VPT>;
+  const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
+  cudaError_t e = allow_smem((const void*)kern);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, 32 * (1 + reducers) + appliers, gain_bytes + stages * stride, s>>>(
+      static_cast<const T*>(a.dy), static_cast<const T*>(a.x), static_cast<const T*>(a.gamma),
+      a.rstd, static_cast<T*>(a.dx), a.partial, a.rows, a.hidden, a.offset ? 1.f : 0.f, stages,
+      reducers);
+  return cudaGetLastError();
+}
+
+template <typename T>
+bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+  constexpr int E = Traits<T>::kVec;
+  const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
+  int stages = 0, reducers = 0;
+  split_stages((kRingBudget - gain_bytes) / stride, &stages, &reducers);
+  if (stages < 3) return false;
+  int appliers = 0;
+  // at most 2 vectors per applier: gains and dw accumulators in registers
+  const int vpt = pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 2, &appliers);
+  if (vpt == 0) return false;
+  const int grid = grid_for(a.rows, a.max_partials, err);
+  if (*err != cudaSuccess) return true;
+  *nparts = grid;
+  if (vpt == 1)
+    *err = launch_bwd_tma_v<T, 1>(a, appliers, stages, reducers, grid, s);
+  else
+    *err = launch_bwd_tma_v<T, 2>(a, appliers, stages, reducers, grid, s);
+  return true;
+}
+
+}  // namespace
+
+bool try_launch_fwd_tma(int dtype, const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
+  if (!a.vec_ok) return false;
+  switch (dtype) {
+    case 0: return try_fwd_tma_t<float>(a, s, err);
+    case 1: return try_fwd_tma_t<__nv_bfloat16>(a, s, err);
+    default: return try_fwd_tma_t<__half>(a, s, err);
+  }
+}
+
+bool try_launch_bwd_tma(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
+                        int* nparts) {
+  if (!a.vec_ok) return false;
+  switch (dtype) {
+    case 0: return try_bwd_tma_t<float>(a, s, err, nparts);
+    case 1: return try_bwd_tma_t<__nv_bfloat16>(a, s, err, nparts);
+    default: return try_bwd_tma_t<__half>(a, s, err, nparts);
+  }
+}
+
+cudaError_t read_wait_timeouts(unsigned int* out) {
+  return cudaMemcpyFromSymbol(out, g_wait_timeouts, sizeof(unsigned int));
+}
+
+}  // namespace rmsn
+
+extern "C" int rms_norm_wait_timeouts(unsigned int* count) {
+  if (!count) return RMSN_ERR_NULL;
+  return rmsn::read_wait_timeouts(count) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
+}

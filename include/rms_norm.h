@@ -131,6 +131,13 @@ int rms_norm_last_cuda_error(void);
  * this thread enqueued (0 when nothing was launched). */
 int rms_norm_last_launch_count(void);
 
+/* The staged kernels bound every wait on a shared-memory barrier (about one
+ * second); a wait that runs out abandons the rest of its CTA's rows, leaving
+ * their outputs unwritten, and is counted on the device.  Writes to *count
+ * how many such waits ran out on the current device since the library was
+ * loaded (0 in correct operation).  Synchronises with the device. */
+int rms_norm_wait_timeouts(unsigned int* count);
+
 /*
  * Backward without caller-provided scratch.  The method's pages describe no
  * such call; it exists for callers that cannot allocate device memory at the

@@ -215,3 +215,8 @@ def test_launch_counts(L):
     assert L.last_launch_count() == 1
     L.rms_norm_bwd(x, x, g, rstd)
     assert L.last_launch_count() == 2
+
+
+def test_no_bounded_wait_ran_out(L):
+    """No bounded wait of the staged kernels timed out during this file."""
+    assert L.wait_timeouts() == 0
