@@ -7,20 +7,29 @@ workload, through the C ABI.  Default workload: Llama-shaped bf16
 activation, 4096 rows (4 x 1024 tokens) x hidden 4096, eps 1e-5, round-once
 store, inputs drawn once (seeded) and resident in HBM.
 
-Printed (rank 0, one JSON line): achieved GB/s of algorithmic bytes over the
-device time of our kernels (CUDA events on the launching stream, L2 flushed
-before every timed call), microseconds per call, the roofline of the
-backward call, an end-to-end number through the public API with host
-buffers, the float64 oracle timed on the host as a baseline, and the SM
-clocks sampled during the timed region.
+Timing.  The batch is copied several times in HBM (at least six L2 sizes
+of data in all) and the steps cycle through the copies, the backward of a
+step reading the copy whose forward ran half a cycle earlier, so every
+kernel reads inputs that the other copies' traffic has evicted from L2.
+The timed steps are captured, as the C-ABI calls they are, in one CUDA
+graph, replayed once between CUDA events with a barrier and a device
+synchronisation on both sides.  The forward and the backward are also timed
+alone (graphs of back-to-back calls) for the per-kernel roofline, and as
+isolated calls after an L2 flush.
+
+Printed (rank 0, one JSON line): achieved GB/s of algorithmic bytes,
+microseconds per call, the roofline of the backward and of the forward, an
+end-to-end number through the public API with host buffers, the float64
+oracle timed on the host as a baseline, and the SM clocks sampled while the
+timed graph ran.
 
 ``--impl reference`` times the oracle instead (rank 0 only, on the host
 cores, on a bounded sample of the same workload).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
 Under torchrun every rank runs the workload on its own GPU (weak scaling:
-the rows of one batch per rank, no collective on the data path); the time
-is the maximum over ranks.
+one batch per rank, no collective on the data path); the time is the
+maximum over ranks.
 """
 from __future__ import annotations
 
@@ -94,7 +103,7 @@ CLOCK_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reaso
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms in the background."""
+    """nvidia-smi sampled every 50 ms in the background."""
 
     def __init__(self, gpu_id: str):
         self.t0 = time.time()
@@ -102,7 +111,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", gpu_id],
+                 "-lms", "50", "-i", gpu_id],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -185,6 +194,8 @@ def time_oracle(w, rows: int):
 
 
 def run_ours(args, rank, world, local):
+    import math
+
     import torch
 
     import bwd_rms_norm_gb300 as L
@@ -197,84 +208,117 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
+    stream = torch.cuda.current_stream(dev)
 
     w = W.all_workloads()[args.workload]
     inp = W.make_inputs(w)
-    x, g, dy = (inp[k].to(dev) for k in ("x", "gamma", "dy"))
-    y = torch.empty_like(x)
-    rstd = torch.empty(w.rows, dtype=torch.float32, device=dev)
-    dx = torch.empty_like(x)
-    dw = torch.empty(w.hidden, dtype=torch.float32, device=dev)
-    ws = torch.empty(L.rms_norm_bwd_workspace_size(w.rows, w.hidden, x.dtype), dtype=torch.uint8,
-                     device=dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
-    flush_elems = 2 * l2 // 4
-    flush = torch.empty(flush_elems, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
-    def call_fwd():
-        L.rms_norm_fwd(x, g, w.eps, w.offset, w.cast_mode, y=y, rstd=rstd)
+    # Several copies of the batch, cycled, so that every step finds its
+    # inputs evicted from L2 by the other copies' traffic (at least six L2
+    # sizes of data in the cycle).
+    set_bytes = 4 * w.rows * w.hidden * w.elem_bytes + 4 * w.rows
+    nsets = max(2, min(8, math.ceil(6 * l2 / set_bytes)))
+    sets = []
+    for _ in range(nsets):
+        x = inp["x"].to(dev)
+        sets.append({"x": x, "dy": inp["dy"].to(dev), "y": torch.empty_like(x),
+                     "dx": torch.empty_like(x),
+                     "rstd": torch.empty(w.rows, dtype=torch.float32, device=dev)})
+    g = inp["gamma"].to(dev)
+    dw = torch.empty(w.hidden, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, L.rms_norm_bwd_workspace_size(w.rows, w.hidden, g.dtype)),
+                     dtype=torch.uint8, device=dev)
+    half = nsets // 2
 
-    def call_bwd():
-        L.rms_norm_bwd(dy, x, g, rstd, w.offset, dx=dx, dw=dw, workspace=ws)
+    def fwd(k):
+        S = sets[k]
+        L.rms_norm_fwd(S["x"], g, w.eps, w.offset, w.cast_mode, y=S["y"], rstd=S["rstd"])
 
-    def l2_flush(i):
-        flush.fill_(i)                 # writes 2x the L2 size
-        torch.cuda._sleep(200_000)     # keeps the GPU busy while the host enqueues
+    def bwd(k):
+        S = sets[k]
+        L.rms_norm_bwd(S["dy"], S["x"], g, S["rstd"], w.offset, dx=S["dx"], dw=dw, workspace=ws)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    def step(i):
+        # the backward works on a copy whose forward ran `half` steps ago
+        fwd(i % nsets)
+        bwd((i + half) % nsets)
 
-    def step(i, evs):
-        l2_flush(2 * i)
-        if evs: evs[0].record(stream)
-        call_fwd()
-        if evs: evs[1].record(stream)
-        l2_flush(2 * i + 1)
-        if evs: evs[2].record(stream)
-        call_bwd()
-        if evs: evs[3].record(stream)
-
-    for i in range(args.warmup):
-        step(i, None)
+    # eager warm-up: every kernel configuration is set up before capture
+    for i in range(max(args.warmup, nsets)):
+        step(i)
     torch.cuda.synchronize()
+
+    def capture(fn, n):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(n):
+                fn(i)
+        return graph
+
+    g_steps = capture(step, args.steps)           # exactly the timed steps
+    reps = 8 * nsets
+    g_fwd = capture(lambda i: fwd(i % nsets), reps)
+    g_bwd = capture(lambda i: bwd(i % nsets), reps)
+    torch.cuda.synchronize()
+
+    def timed(graph, times):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(times):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    # graph warm-up, then per-kernel averages over back-to-back launches
+    for _ in range(max(3, args.warmup // 4)):
+        g_fwd.replay()
+        g_bwd.replay()
+    fwd_us = min(timed(g_fwd, 4) for _ in range(3)) * 1e3 / (4 * reps)
+    bwd_us = min(timed(g_bwd, 4) for _ in range(3)) * 1e3 / (4 * reps)
 
     uuid = str(getattr(props, "uuid", "")) or str(local)
     sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.isdigit() else uuid)
-    # let the sampler start and the clocks settle on the same work
     t_soak = time.time()
-    while time.time() - t_soak < 0.5:
-        for i in range(20):
-            step(i, None)
+    while time.time() - t_soak < 0.6:      # clocks settle on the same work
+        g_fwd.replay()
+        g_bwd.replay()
         torch.cuda.synchronize()
 
     barrier(world)
     torch.cuda.synchronize()
     t_start = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        step(i, ev[i])
+    e0.record(stream)
+    g_steps.replay()
+    e1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     barrier(world)
     t_end = time.time()
     sampler.mark(t_start, t_end)
+    step_ms = e0.elapsed_time(e1)
+    step_ms = reduce_max(step_ms, world, dev)
+    # keep sampling a little after the timed region so that short regions
+    # still get a sample taken under the same load
+    t_tail = time.time()
+    while time.time() - t_tail < 0.3:
+        g_steps.replay()
+        torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    bwd_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    kern_ms = sum(fwd_ms) + sum(bwd_ms)
-    kern_ms = reduce_max(kern_ms, world, dev)
-    ms_per_step = kern_ms / args.steps
+    ms_per_step = step_ms / args.steps
     total_bytes = w.step_bytes() * args.steps * world
-    value = total_bytes / (kern_ms * 1e-3) / 1e9
+    value = total_bytes / (step_ms * 1e-3) / 1e9
 
     peak, peak_src = measured_peak_gbs()
-    bwd_avg_s = statistics.mean(bwd_ms) * 1e-3
-    fwd_avg_s = statistics.mean(fwd_ms) * 1e-3
-    bwd_ach = w.bwd_bytes() / bwd_avg_s / 1e9
-    fwd_ach = w.fwd_bytes() / fwd_avg_s / 1e9
+    fwd_ach = w.fwd_bytes() / (fwd_us * 1e-6) / 1e9
+    bwd_ach = w.bwd_bytes() / (bwd_us * 1e-6) / 1e9
     traffic = load_traffic(args.workload)
+    iso = isolated_calls(fwd, bwd, nsets, dev, l2)
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(L, w, inp, dev, args.e2e_steps)
@@ -286,9 +330,9 @@ def run_ours(args, rank, world, local):
         # host time have been spent
         secs, nbytes, passes = 0.0, 0, 0
         while secs < 10.0 and passes < 50:
-            s, b = time_oracle(w, w.rows)
-            secs += s
-            nbytes += b
+            s_, b_ = time_oracle(w, w.rows)
+            secs += s_
+            nbytes += b_
             passes += 1
         cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1,
                "kind": "oracle",
@@ -306,21 +350,22 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == "bf16" else w.dtype,
+        "dtype": w.dtype,
         "data": "synthetic (seeded, see workloads/)",
         "config": {
             "workload": args.workload, "rows": w.rows, "hidden": w.hidden, "eps": w.eps,
             "offset": w.offset, "cast_mode": w.cast_mode, "stats": "fp32", "rstd": "fp32",
             "dw": "fp32", "global_batch_rows": w.rows * world,
-            "parallelism": f"replica x{world} (rows per rank)",
-            "l2": "flushed before every timed call (write of 2x L2)",
-            "timing": "CUDA events around each C-ABI call on its stream; value = bytes / sum of event times",
+            "parallelism": f"replica x{world} (one batch per rank)",
+            "l2": (f"inputs larger than L2: {nsets} copies of the batch "
+                   f"({nsets * set_bytes / 2**20:.0f} MiB) cycled; each step's backward "
+                   f"reads the copy whose forward ran {half} steps earlier"),
+            "timing": ("CUDA events around one CUDA-graph replay of exactly `steps` "
+                       "forward+backward steps (C-ABI calls captured in order)"),
             "algorithmic_bytes_per_step": w.step_bytes(),
         },
-        "fwd_us": round(statistics.mean(fwd_ms) * 1e3, 3),
-        "bwd_us": round(statistics.mean(bwd_ms) * 1e3, 3),
-        "fwd_us_median": round(statistics.median(fwd_ms) * 1e3, 3),
-        "bwd_us_median": round(statistics.median(bwd_ms) * 1e3, 3),
+        "fwd_us": round(fwd_us, 3),
+        "bwd_us": round(bwd_us, 3),
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         "peak_source": f"{peak_src} HBM {peak} GB/s",
         "roofline": {
@@ -329,12 +374,14 @@ def run_ours(args, rank, world, local):
             "frac": round(bwd_ach / peak, 4),
             "traffic": traffic.get("bwd"),
             "algorithmic_bytes": w.bwd_bytes(),
+            "timing": f"{4 * reps} back-to-back backward calls in a CUDA graph, best of 3",
         },
         "roofline_fwd": {
             "kernel": "rms_norm_fwd", "bound": "hbm", "achieved": round(fwd_ach, 1),
             "peak": peak, "unit": "GB/s", "frac": round(fwd_ach / peak, 4),
             "traffic": traffic.get("fwd"), "algorithmic_bytes": w.fwd_bytes(),
         },
+        "isolated_call": iso,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
@@ -344,6 +391,29 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def isolated_calls(fwd, bwd, nsets, dev, l2, n=200):
+    """Microseconds of single calls, each preceded by a write of twice the L2
+    size and a short device-side sleep (so the host is ahead), timed with
+    CUDA events around the call: the latency of a call made alone."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev)
+    out = {}
+    for name, fn in (("fwd_us", fwd), ("bwd_us", bwd)):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for i in range(n):
+            flush.fill_(i)
+            torch.cuda._sleep(200_000)
+            ev[i][0].record(stream)
+            fn(i % nsets)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        out[name] = round(statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3, 3)
+    out["timing"] = "median of 200 calls, L2 flushed (write of 2x L2) before each"
+    return out
 
 
 def reduce_max_rate(rate: float, world: int, dev) -> float:
@@ -461,7 +531,7 @@ def run_reference(args, rank, world, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

@@ -62,11 +62,10 @@ __global__ void __launch_bounds__(1024) bwd_cta_rows(
     int64_t rows, int hidden, float off) {
   constexpr int E = Traits<T>::kVec;
   __shared__ float red[64];
-#if __CUDA_ARCH__ >= 900
   // Let the finalize kernel be scheduled now; it waits for this grid to
   // complete before reading the partials.
-  cudaTriggerProgrammaticLaunchCompletion();
-#endif
+  pdl_trigger();
+  pdl_wait();
   const int nvec = hidden / E;
   const int64_t r0 = (int64_t)blockIdx.x * rows / gridDim.x;
   const int64_t r1 = (int64_t)(blockIdx.x + 1) * rows / gridDim.x;
@@ -158,9 +157,8 @@ __global__ void __launch_bounds__(256) bwd_scalar(
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
     int64_t rows, int hidden, float off) {
   __shared__ float red[64];
-#if __CUDA_ARCH__ >= 900
-  cudaTriggerProgrammaticLaunchCompletion();
-#endif
+  pdl_trigger();
+  pdl_wait();
   const int64_t r0 = (int64_t)blockIdx.x * rows / gridDim.x;
   const int64_t r1 = (int64_t)(blockIdx.x + 1) * rows / gridDim.x;
   float* pr = partial + (int64_t)blockIdx.x * hidden;
@@ -195,9 +193,8 @@ __global__ void __launch_bounds__(256) bwd_scalar(
 __global__ void __launch_bounds__(1024) dw_finalize(const float* __restrict__ partial,
                                                     float* __restrict__ dw, int nparts,
                                                     int hidden) {
-#if __CUDA_ARCH__ >= 900
-  cudaGridDependencySynchronize();
-#endif
+  pdl_trigger();
+  pdl_wait();
   __shared__ float s[32][33];
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int j = blockIdx.x * 32 + tx;
@@ -218,17 +215,8 @@ __global__ void __launch_bounds__(1024) dw_finalize(const float* __restrict__ pa
 
 cudaError_t launch_finalize(const float* partial, float* dw, int nparts, int hidden,
                             cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((hidden + 31) / 32));
-  cfg.blockDim = dim3(32, 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, dw_finalize, partial, dw, nparts, hidden);
+  return launch_kernel(dw_finalize, dim3((unsigned)((hidden + 31) / 32)), dim3(32, 32), 0, s, 1,
+                       partial, dw, nparts, hidden);
 }
 
 template <typename T, int VPT>
@@ -242,11 +230,10 @@ cudaError_t launch_rows(const BwdArgs& a, int tpr, cudaStream_t s, int* nparts) 
   if (g > a.rows) g = a.rows;
   if (g > a.max_partials) g = a.max_partials;
   *nparts = (int)g;
-  kern<<<(unsigned)g, tpr, 0, s>>>(
-      static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
-      static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial, a.rows,
-      a.hidden, a.offset ? 1.f : 0.f);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3((unsigned)g), dim3(tpr), 0, s, 1,
+                       static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
+                       static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
+                       a.rows, a.hidden, a.offset ? 1.f : 0.f);
 }
 
 template <typename T> int dtype_code();
@@ -287,11 +274,10 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s, int* launches) {
     if (g > a.rows) g = a.rows;
     if (g > a.max_partials) g = a.max_partials;
     nparts = (int)g;
-    kern<<<(unsigned)g, 256, 0, s>>>(
-        static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
-        static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial, a.rows,
-        a.hidden, a.offset ? 1.f : 0.f);
-    e = cudaGetLastError();
+    e = launch_kernel(kern, dim3((unsigned)g), dim3(256), 0, s, 1,
+                      static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
+                      static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
+                      a.rows, a.hidden, a.offset ? 1.f : 0.f);
   }
   if (e != cudaSuccess) return e;
   *launches += 1;

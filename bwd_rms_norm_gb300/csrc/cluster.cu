@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(512) fwd_cluster(
   // every CTA of the cluster must be running before any writes into its
   // shared memory
   cluster_sync();
+  pdl_trigger();
+  pdl_wait();
   uint4 xv[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
@@ -126,9 +128,8 @@ __global__ void __launch_bounds__(512, 1) bwd_cluster(
   constexpr int E = Traits<T>::kVec;
   __shared__ float red[64];
   __shared__ float slots[2 * kMaxCluster];
-#if __CUDA_ARCH__ >= 900
-  cudaTriggerProgrammaticLaunchCompletion();
-#endif
+  pdl_trigger();
+  pdl_wait();
   const uint32_t rank = cta_rank();
   const int64_t cid = blockIdx.x / csize;
   const int64_t nclusters = gridDim.x / csize;
@@ -257,9 +258,7 @@ cudaError_t launch_clustered(K kern, unsigned grid, unsigned block, int csize, c
                              Args... args) {
   cudaError_t e = allow_cluster((const void*)kern, csize);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config(grid, block, csize, s, attr);
-  return cudaLaunchKernelEx(&cfg, kern, args...);
+  return launch_kernel(kern, dim3(grid), dim3(block), 0, s, csize, args...);
 }
 
 struct ClusterOcc {

@@ -150,6 +150,17 @@ __device__ __forceinline__ float block_sum(float v, float* red, int parity) {
   return s;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// so that it may start while the previous kernel on the stream finishes;
+// pdl_wait() blocks until that kernel has completed and its memory writes
+// are visible, so a kernel calls it before its first global memory access.
+// pdl_trigger() lets the next kernel on the stream be scheduled; it only
+// runs its own prologue before its own pdl_wait().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Correctly rounded 1/sqrt(v).
 __device__ __forceinline__ float rstd_of(float mean_sq, float eps) {
   return __frsqrt_rn(mean_sq + eps);

@@ -45,7 +45,9 @@ __global__ void __launch_bounds__(256) fwd_warp_rows(
   constexpr int E = Traits<T>::kVec;
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  pdl_trigger();
   if (row >= rows) return;  // whole warps leave together
+  pdl_wait();
   const int nvec = hidden / E;
   const T* xr = x + row * hidden;
   T* yr = y + row * hidden;
@@ -89,6 +91,8 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) fwd_cta_row(
   const int nvec = hidden / E;
   const T* xr = x + row * hidden;
   T* yr = y + row * hidden;
+  pdl_trigger();
+  pdl_wait();
 
   uint4 xv[VPT];
 #pragma unroll
@@ -127,6 +131,8 @@ __global__ void __launch_bounds__(256) fwd_scalar(
   const int64_t row = blockIdx.x;
   const T* xr = x + row * hidden;
   T* yr = y + row * hidden;
+  pdl_trigger();
+  pdl_wait();
   float ss = 0.f;
   for (int j = threadIdx.x; j < hidden; j += blockDim.x) {
     const float f = Traits<T>::to_f(xr[j]);
@@ -162,18 +168,19 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
   T* y = static_cast<T*>(a.y);
   const float off = a.offset ? 1.f : 0.f;
   const int nvec = a.hidden / E;
+  cudaError_t e = cudaSuccess;
 
   if (a.vec_ok && nvec <= 128) {
     // one warp per row, 8 rows per CTA
     const int vpt = pow2_at_least((nvec + 31) / 32);
     const int64_t grid = (a.rows + 7) / 8;
     switch (vpt) {
-      case 1: fwd_warp_rows<T, 1><<<(unsigned)grid, 256, 0, s>>>(x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
-      case 2: fwd_warp_rows<T, 2><<<(unsigned)grid, 256, 0, s>>>(x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
-      default: fwd_warp_rows<T, 4><<<(unsigned)grid, 256, 0, s>>>(x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      case 1: e = launch_kernel(fwd_warp_rows<T, 1>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      case 2: e = launch_kernel(fwd_warp_rows<T, 2>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      default: e = launch_kernel(fwd_warp_rows<T, 4>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
     }
-    *launches += 1;
-    return cudaGetLastError();
+    if (e == cudaSuccess) *launches += 1;
+    return e;
   }
   if (a.vec_ok) {
     // one CTA per row; up to 4 vectors per thread at 1024 threads, 8 or 16
@@ -184,24 +191,24 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
     if (tpr <= (vpt >= 8 ? 512 : 1024)) {
       const unsigned grid = (unsigned)a.rows;
       switch (vpt) {
-        case 1: fwd_cta_row<T, 1><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
-        case 2: fwd_cta_row<T, 2><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
-        case 4: fwd_cta_row<T, 4><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
-        case 8: fwd_cta_row<T, 8><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
-        default: fwd_cta_row<T, 16><<<grid, tpr, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        case 1: e = launch_kernel(fwd_cta_row<T, 1>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        case 2: e = launch_kernel(fwd_cta_row<T, 2>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        case 4: e = launch_kernel(fwd_cta_row<T, 4>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        case 8: e = launch_kernel(fwd_cta_row<T, 8>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        default: e = launch_kernel(fwd_cta_row<T, 16>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
       }
-      *launches += 1;
-      return cudaGetLastError();
+      if (e == cudaSuccess) *launches += 1;
+      return e;
     }
   }
-  cudaError_t e = cudaSuccess;
   if (try_launch_fwd_cluster(dtype_code<T>(), a, s, &e)) {
     if (e == cudaSuccess) *launches += 1;
     return e;
   }
-  fwd_scalar<T><<<(unsigned)a.rows, 256, 0, s>>>(x, g, y, a.rstd, a.hidden, a.eps, off, a.twice);
-  *launches += 1;
-  return cudaGetLastError();
+  e = launch_kernel(fwd_scalar<T>, dim3((unsigned)a.rows), dim3(256), 0, s, 1, x, g, y, a.rstd,
+                    a.hidden, a.eps, off, a.twice);
+  if (e == cudaSuccess) *launches += 1;
+  return e;
 }
 
 }  // namespace

@@ -55,6 +55,33 @@ bool try_launch_fwd_cluster(int dtype, const FwdArgs& a, cudaStream_t s, cudaErr
 bool try_launch_bwd_cluster(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
                             int* nparts);
 
+// Launch `kern` with programmatic dependent launch allowed (see pdl_wait in
+// common.cuh) and, when `cluster` > 1, thread-block clusters of `cluster`
+// CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, int cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Device properties, cached per device.
 int sm_count(int device);
 int max_blocks_per_sm(const void* func, int block, size_t smem);

@@ -246,6 +246,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = hidden / E;
@@ -342,11 +344,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   constexpr int E = Traits<T>::kVec;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Pipe pipe;
-#if __CUDA_ARCH__ >= 900
-  // Let the finalize kernel be scheduled now; it waits for this grid to
-  // complete before reading the partials.
-  cudaTriggerProgrammaticLaunchCompletion();
-#endif
   const int row_bytes = hidden * (int)sizeof(T);
   const int stride = (2 * row_bytes + 127) / 128 * 128;
   const int gain_bytes = (hidden * 4 + 127) / 128 * 128;
@@ -357,6 +354,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
+  // the next kernel (the dw finalize) may be scheduled now; it waits for
+  // this grid to complete before reading the partials
+  pdl_trigger();
+  pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = hidden / E;
@@ -400,9 +401,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
           gf[e + 3] = q.w;
         }
 #pragma unroll
-        for (int e = 0; e < E; ++e) part[e] = fmaf(df[e] * gf[e], xf[e] * rs, part[e]);
+        for (int e = 0; e < E; ++e) part[e] = fmaf(df[e] * gf[e], xf[e], part[e]);
       }
-      const float dot = warp_sum(pairwise<E>(part));
+      // sum(g * x) * rstd: the row's rstd is applied once, to the sum
+      const float dot = warp_sum(pairwise<E>(part)) * rs;
       if (lane == 0) {
         pipe.stat[pos.stage] = dot / (float)hidden;
         mbar_arrive(&pipe.red[pos.stage]);
@@ -509,9 +511,18 @@ void split_stages(int fit, int* stages, int* reducers) {
   if (fit <= kMaxReducers) {
     *stages = fit;
     *reducers = fit;
-  } else {
-    *reducers = 8;
-    *stages = fit / 8 * 8;
+    return;
+  }
+  // the most stages that some reducer count from 8 to 12 divides; among
+  // equals, the most reducers (a row's reduction is on the critical path of
+  // its outputs, so more reducers beat a few more stages)
+  *stages = 0;
+  for (int r = 8; r <= kMaxReducers; ++r) {
+    const int st = fit / r * r;
+    if (st >= *stages) {
+      *stages = st;
+      *reducers = r;
+    }
   }
 }
 
@@ -531,10 +542,10 @@ cudaError_t launch_fwd_tma_v(const FwdArgs& a, int appliers, int stages, int red
   const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   cudaError_t e = allow_smem((const void*)kern);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 32 * (1 + reducers) + appliers, stages * stride, s>>>(
-      static_cast<const T*>(a.x), static_cast<const T*>(a.gamma), static_cast<T*>(a.y), a.rstd,
-      a.rows, a.hidden, a.eps, a.offset ? 1.f : 0.f, a.twice, stages, reducers);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(32 * (1 + reducers) + appliers),
+                       (size_t)stages * stride, s, 1, static_cast<const T*>(a.x),
+                       static_cast<const T*>(a.gamma), static_cast<T*>(a.y), a.rstd, a.rows,
+                       a.hidden, a.eps, a.offset ? 1.f : 0.f, a.twice, stages, reducers);
 }
 
 template <typename T>
@@ -566,11 +577,11 @@ cudaError_t launch_bwd_tma_v(const BwdArgs& a, int appliers, int stages, int red
   const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
   cudaError_t e = allow_smem((const void*)kern);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 32 * (1 + reducers) + appliers, gain_bytes + stages * stride, s>>>(
-      static_cast<const T*>(a.dy), static_cast<const T*>(a.x), static_cast<const T*>(a.gamma),
-      a.rstd, static_cast<T*>(a.dx), a.partial, a.rows, a.hidden, a.offset ? 1.f : 0.f, stages,
-      reducers);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(32 * (1 + reducers) + appliers),
+                       (size_t)gain_bytes + (size_t)stages * stride, s, 1,
+                       static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
+                       static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
+                       a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers);
 }
 
 template <typename T>
