@@ -211,6 +211,8 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
 
     w = W.all_workloads()[args.workload]
+    if args.rows:
+        w = w.with_(rows=args.rows)
     inp = W.make_inputs(w)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
@@ -353,7 +355,8 @@ def run_ours(args, rank, world, local):
         "dtype": w.dtype,
         "data": "synthetic (seeded, see workloads/)",
         "config": {
-            "workload": args.workload, "rows": w.rows, "hidden": w.hidden, "eps": w.eps,
+            "workload": args.workload + (f" (rows overridden to {w.rows})" if args.rows else ""),
+            "rows": w.rows, "hidden": w.hidden, "eps": w.eps,
             "offset": w.offset, "cast_mode": w.cast_mode, "stats": "fp32", "rstd": "fp32",
             "dw": "fp32", "global_batch_rows": w.rows * world,
             "parallelism": f"replica x{world} (one batch per rank)",
@@ -467,16 +470,34 @@ def run_e2e(L, w, inp, dev, steps: int):
             "timing": "wall clock over steps, synchronised at both ends"}
 
 
+def sources_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the CUDA sources (file names and
+    contents, sorted), to tell whether committed counters still describe
+    the kernels being run."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "bwd_rms_norm_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it covers the
-    current kernels of this workload (see profiles/)."""
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/traffic.json), or {} when it does not cover this workload or
+    was taken on kernels other than the ones built from the current
+    sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            data = json.load(f)
-        return data.get(workload, {})
+            data = json.load(f).get(workload, {})
     except (OSError, ValueError):
         return {}
+    if data.get("sources_sha256_16") != sources_hash():
+        return {}
+    return data
 
 
 # ---------------------------------------------------------------------------
@@ -535,6 +556,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the workload's row count (profiling a larger case)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

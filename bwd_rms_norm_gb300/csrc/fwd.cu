@@ -160,6 +160,9 @@ int pow2_at_least(int v) {
   return p;
 }
 
+// Rows of up to this many 16-byte vectors run one warp per row.
+constexpr int kWarpRowMaxVec = 128;
+
 template <typename T>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
   constexpr int E = Traits<T>::kVec;
@@ -170,22 +173,28 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
   const int nvec = a.hidden / E;
   cudaError_t e = cudaSuccess;
 
-  if (a.vec_ok && nvec <= 128) {
+  if (a.vec_ok && nvec <= kWarpRowMaxVec) {
     // one warp per row, 8 rows per CTA
     const int vpt = pow2_at_least((nvec + 31) / 32);
     const int64_t grid = (a.rows + 7) / 8;
     switch (vpt) {
       case 1: e = launch_kernel(fwd_warp_rows<T, 1>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
       case 2: e = launch_kernel(fwd_warp_rows<T, 2>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
-      default: e = launch_kernel(fwd_warp_rows<T, 4>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      case 4: e = launch_kernel(fwd_warp_rows<T, 4>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      case 8: e = launch_kernel(fwd_warp_rows<T, 8>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      default: e = launch_kernel(fwd_warp_rows<T, 16>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
     }
     if (e == cudaSuccess) *launches += 1;
     return e;
   }
   if (a.vec_ok) {
-    // one CTA per row; up to 4 vectors per thread at 1024 threads, 8 or 16
-    // at 512 threads (the register file holds the whole row)
-    int vpt = pow2_at_least((nvec + 255) / 256);
+    // one CTA per row of about 128 threads with up to 4 vectors each (a
+    // 4-warp reduction per row, 4 loads in flight per thread); wider rows
+    // use more threads, and rows too wide for 1024 threads x 4 vectors use
+    // 8 or 16 vectors per thread at 512 threads
+    int vpt = pow2_at_least((nvec + 127) / 128);
+    if (vpt > 4) vpt = 4;
+    if ((nvec + vpt - 1) / vpt > 1024) vpt = pow2_at_least((nvec + 511) / 512);
     if (vpt > 16) vpt = 16;
     const int tpr = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
     if (tpr <= (vpt >= 8 ? 512 : 1024)) {

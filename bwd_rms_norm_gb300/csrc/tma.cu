@@ -95,6 +95,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep until the phase completes or
+// about `hint_ns` pass, so that waiting warps leave the issue slots to the
+// warps that have work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // 1D bulk copy global -> this CTA's shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
@@ -110,8 +126,7 @@ __device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) 
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
     if (*abort) return false;
     if (global_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
@@ -372,9 +387,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   }
 
   if (warp <= reducers) {
-    // the reducers stage the fp32 gains while the first copies are in flight
-    for (int j = threadIdx.x - 32; j < hidden; j += 32 * reducers)
-      gain[j] = Traits<T>::to_f(gamma[j]) + off;
+    // The reducers stage the fp32 gains.  Vector v's E gains are stored as
+    // E/4 float4 in E/4 planes of nvec float4 each (plane q holds elements
+    // 4q..4q+3 of every vector), so that a warp reading the planes of 32
+    // consecutive vectors reads 512 contiguous bytes: no bank conflicts.
+    for (int j = threadIdx.x - 32; j < hidden; j += 32 * reducers) {
+      const int v = j / E, e = j % E;
+      gain[((e / 4) * nvec + v) * 4 + (e % 4)] = Traits<T>::to_f(gamma[j]) + off;
+    }
     asm volatile("bar.sync 1, %0;" ::"r"(32 * reducers) : "memory");
     const float4* g4 = reinterpret_cast<const float4*>(gain);
     const int d = warp - 1;
@@ -394,7 +414,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
         unpack<T>(st[doff + v], df);
 #pragma unroll
         for (int e = 0; e < E; e += 4) {
-          const float4 q = g4[(v * E + e) / 4];
+          const float4 q = g4[(e / 4) * nvec + v];
           gf[e] = q.x;
           gf[e + 1] = q.y;
           gf[e + 2] = q.z;
