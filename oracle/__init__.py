@@ -17,7 +17,13 @@ Parity status of each function (what pins it is in ``tests/test_oracle.py``):
 * ``rms_norm.backward`` / ``backward_exact`` -- pinned: central finite
   differences of sum(dy * y) in float64, torch autograd through CPU
   ``rms_norm`` in float64, the orthogonality of dx to x at eps = 0.
+* ``layer_norm.forward`` / ``backward`` (and the ``_exact`` forms) -- pinned
+  in ``tests/test_oracle_layer_norm.py``: torch's CPU ``layer_norm`` in
+  float64 and its autograd, finite differences, shift invariance of dx,
+  zero mean and the variance identity of x_hat, torch's CPU bf16
+  ``layer_norm``.
 """
+from . import layer_norm  # noqa: F401
 from .rounding import FORMATS, max_finite, round_to, ulp_distance  # noqa: F401
 from .rms_norm import (  # noqa: F401
     BF16,
