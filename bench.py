@@ -23,6 +23,9 @@ end-to-end number through the public API with host buffers, the float64
 oracle timed on the host as a baseline, and the SM clocks sampled while the
 timed graph ran.
 
+``--workload ln_...`` runs the LayerNorm entry points the same way (one
+step = layer_norm_fwd + layer_norm_bwd).
+
 ``--impl reference`` times the oracle instead (rank 0 only, on the host
 cores, on a bounded sample of the same workload).
 
@@ -46,6 +49,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "RMSNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
+METRIC_LN = "LayerNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
 DEFAULT_WORKLOAD = "llama_bf16_4096x4096"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -176,20 +180,36 @@ def measured_peak_gbs():
 _ORACLE_INPUTS = {}
 
 
+def workload_by_name(name: str):
+    """RMSNorm workloads and the LayerNorm ones (names starting ``ln_``)."""
+    import workloads as W
+    table = dict(W.all_workloads())
+    table.update(W.layer_norm_workloads())
+    if name not in table:
+        raise SystemExit(f"unknown workload {name!r}; known: {', '.join(sorted(table))}")
+    return table[name]
+
+
 def time_oracle(w, rows: int):
     """Seconds for one oracle forward + backward over ``rows`` rows of ``w``
     (inputs drawn once per row count, outside the timing)."""
     import workloads as W
+    from oracle import layer_norm as oln
     from oracle import rms_norm as orm
     ws = w.with_(rows=rows)
     if (ws.name, rows) not in _ORACLE_INPUTS:
         _ORACLE_INPUTS.clear()
         inp = W.make_inputs(ws)
-        _ORACLE_INPUTS[(ws.name, rows)] = tuple(W.as_float64(inp[k]) for k in ("x", "gamma", "dy"))
-    xd, gd, dyd = _ORACLE_INPUTS[(ws.name, rows)]
+        _ORACLE_INPUTS[(ws.name, rows)] = tuple(
+            W.as_float64(inp[k]) if k in inp else None for k in ("x", "gamma", "dy", "beta"))
+    xd, gd, dyd, bd = _ORACLE_INPUTS[(ws.name, rows)]
     t = time.perf_counter()
-    _, rstd = orm.forward(xd, gd, ws.eps, ws.offset, ws.dtype, ws.cast_mode)
-    orm.backward(dyd, xd, gd, rstd, ws.offset, ws.dtype)
+    if ws.kind == "ln":
+        _, mean, rstd = oln.forward(xd, gd, bd, ws.eps, ws.dtype)
+        oln.backward(dyd, xd, gd, mean, rstd, ws.dtype)
+    else:
+        _, rstd = orm.forward(xd, gd, ws.eps, ws.offset, ws.dtype, ws.cast_mode)
+        orm.backward(dyd, xd, gd, rstd, ws.offset, ws.dtype)
     return time.perf_counter() - t, ws.step_bytes()
 
 
@@ -210,9 +230,10 @@ def run_ours(args, rank, world, local):
     dist_init(world, "nccl")
     stream = torch.cuda.current_stream(dev)
 
-    w = W.all_workloads()[args.workload]
+    w = workload_by_name(args.workload)
     if args.rows:
         w = w.with_(rows=args.rows)
+    ln = w.kind == "ln"
     inp = W.make_inputs(w)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
@@ -220,27 +241,38 @@ def run_ours(args, rank, world, local):
     # Several copies of the batch, cycled, so that every step finds its
     # inputs evicted from L2 by the other copies' traffic (at least six L2
     # sizes of data in the cycle).
-    set_bytes = 4 * w.rows * w.hidden * w.elem_bytes + 4 * w.rows
+    set_bytes = 4 * w.rows * w.hidden * w.elem_bytes + (8 if ln else 4) * w.rows
     nsets = max(2, min(8, math.ceil(6 * l2 / set_bytes)))
     sets = []
     for _ in range(nsets):
         x = inp["x"].to(dev)
         sets.append({"x": x, "dy": inp["dy"].to(dev), "y": torch.empty_like(x),
                      "dx": torch.empty_like(x),
-                     "rstd": torch.empty(w.rows, dtype=torch.float32, device=dev)})
+                     "rstd": torch.empty(w.rows, dtype=torch.float32, device=dev),
+                     "mean": torch.empty(w.rows, dtype=torch.float32, device=dev)})
     g = inp["gamma"].to(dev)
+    beta = inp["beta"].to(dev) if "beta" in inp else None
     dw = torch.empty(w.hidden, dtype=torch.float32, device=dev)
-    ws = torch.empty(max(16, L.rms_norm_bwd_workspace_size(w.rows, w.hidden, g.dtype)),
-                     dtype=torch.uint8, device=dev)
+    db = torch.empty(w.hidden, dtype=torch.float32, device=dev)
+    ws_fn = L.layer_norm_bwd_workspace_size if ln else L.rms_norm_bwd_workspace_size
+    ws = torch.empty(max(16, ws_fn(w.rows, w.hidden, g.dtype)), dtype=torch.uint8, device=dev)
     half = nsets // 2
 
     def fwd(k):
         S = sets[k]
-        L.rms_norm_fwd(S["x"], g, w.eps, w.offset, w.cast_mode, y=S["y"], rstd=S["rstd"])
+        if ln:
+            L.layer_norm_fwd(S["x"], g, beta, w.eps, y=S["y"], mean=S["mean"], rstd=S["rstd"])
+        else:
+            L.rms_norm_fwd(S["x"], g, w.eps, w.offset, w.cast_mode, y=S["y"], rstd=S["rstd"])
 
     def bwd(k):
         S = sets[k]
-        L.rms_norm_bwd(S["dy"], S["x"], g, S["rstd"], w.offset, dx=S["dx"], dw=dw, workspace=ws)
+        if ln:
+            L.layer_norm_bwd(S["dy"], S["x"], g, S["mean"], S["rstd"], dx=S["dx"], dgamma=dw,
+                             dbeta=db, workspace=ws)
+        else:
+            L.rms_norm_bwd(S["dy"], S["x"], g, S["rstd"], w.offset, dx=S["dx"], dw=dw,
+                           workspace=ws)
 
     def step(i):
         # the backward works on a copy whose forward ran `half` steps ago
@@ -250,6 +282,12 @@ def run_ours(args, rank, world, local):
     # eager warm-up: every kernel configuration is set up before capture
     for i in range(max(args.warmup, nsets)):
         step(i)
+    torch.cuda.synchronize()
+    # kernels one step launches, as the library counts them
+    fwd(0)
+    launches_per_step = L.last_launch_count()
+    bwd(0)
+    launches_per_step += L.last_launch_count()
     torch.cuda.synchronize()
 
     def capture(fn, n):
@@ -323,7 +361,7 @@ def run_ours(args, rank, world, local):
     iso = isolated_calls(fwd, bwd, nsets, dev, l2)
 
     # end to end through the public API: pinned host inputs in, results out
-    e2e = run_e2e(L, w, inp, dev, args.e2e_steps)
+    e2e = run_e2e(L, w, inp, dev, args.e2e_steps, beta is not None)
     e2e["value"] = reduce_max_rate(e2e["value"], world, dev)
 
     cpu = None
@@ -341,8 +379,9 @@ def run_ours(args, rank, world, local):
                "sample": f"{args.workload}: {passes} float64 forward+backward passes over all "
                          f"{w.rows} rows ({secs:.1f} s, numpy, single thread)"}
 
+    op = "layer_norm" if ln else "rms_norm"
     line = {
-        "metric": METRIC,
+        "metric": METRIC_LN if ln else METRIC,
         "value": round(value, 1),
         "unit": "GB/s",
         "n_gpus": world,
@@ -357,8 +396,9 @@ def run_ours(args, rank, world, local):
         "config": {
             "workload": args.workload + (f" (rows overridden to {w.rows})" if args.rows else ""),
             "rows": w.rows, "hidden": w.hidden, "eps": w.eps,
-            "offset": w.offset, "cast_mode": w.cast_mode, "stats": "fp32", "rstd": "fp32",
-            "dw": "fp32", "global_batch_rows": w.rows * world,
+            **({"bias": beta is not None, "mean": "fp32", "dbeta": "fp32"} if ln else
+               {"offset": w.offset, "cast_mode": w.cast_mode}),
+            "stats": "fp32", "rstd": "fp32", "dw": "fp32", "global_batch_rows": w.rows * world,
             "parallelism": f"replica x{world} (one batch per rank)",
             "l2": (f"inputs larger than L2: {nsets} copies of the batch "
                    f"({nsets * set_bytes / 2**20:.0f} MiB) cycled; each step's backward "
@@ -372,7 +412,7 @@ def run_ours(args, rank, world, local):
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         "peak_source": f"{peak_src} HBM {peak} GB/s",
         "roofline": {
-            "kernel": "rms_norm_bwd (row kernel + dw finalize)",
+            "kernel": f"{op}_bwd (row kernel + fixed-order column sums)",
             "bound": "hbm", "achieved": round(bwd_ach, 1), "peak": peak, "unit": "GB/s",
             "frac": round(bwd_ach / peak, 4),
             "traffic": traffic.get("bwd"),
@@ -380,13 +420,13 @@ def run_ours(args, rank, world, local):
             "timing": f"{4 * reps} back-to-back backward calls in a CUDA graph, best of 3",
         },
         "roofline_fwd": {
-            "kernel": "rms_norm_fwd", "bound": "hbm", "achieved": round(fwd_ach, 1),
+            "kernel": f"{op}_fwd", "bound": "hbm", "achieved": round(fwd_ach, 1),
             "peak": peak, "unit": "GB/s", "frac": round(fwd_ach / peak, 4),
             "traffic": traffic.get("fwd"), "algorithmic_bytes": w.fwd_bytes(),
         },
         "isolated_call": iso,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
     }
@@ -427,32 +467,41 @@ def reduce_max_rate(rate: float, world: int, dev) -> float:
     return world / t
 
 
-def run_e2e(L, w, inp, dev, steps: int):
+def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
     """GB/s of algorithmic bytes when every step copies the inputs from
     pinned host memory, runs forward and backward through the Python API and
     copies every result back to pinned host memory."""
     import torch
-    hx, hg, hdy = (inp[k].pin_memory() for k in ("x", "gamma", "dy"))
-    hy = torch.empty_like(hx).pin_memory()
-    hdx = torch.empty_like(hx).pin_memory()
-    hr = torch.empty(w.rows, dtype=torch.float32).pin_memory()
-    hdw = torch.empty(w.hidden, dtype=torch.float32).pin_memory()
-    x = torch.empty_like(hx, device=dev)
-    g = torch.empty_like(hg, device=dev)
-    dy = torch.empty_like(hdy, device=dev)
-    ws = torch.empty(L.rms_norm_bwd_workspace_size(w.rows, w.hidden, x.dtype), dtype=torch.uint8,
+    ln = w.kind == "ln"
+    names = ("x", "gamma", "dy") + (("beta",) if ln and with_beta else ())
+    host_in = {k: inp[k].pin_memory() for k in names}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    hy = torch.empty_like(host_in["x"]).pin_memory()
+    hdx = torch.empty_like(host_in["x"]).pin_memory()
+    stats = [torch.empty(w.rows, dtype=torch.float32).pin_memory() for _ in range(2 if ln else 1)]
+    grads = [torch.empty(w.hidden, dtype=torch.float32).pin_memory()
+             for _ in range(2 if ln and with_beta else 1)]
+    ws_fn = L.layer_norm_bwd_workspace_size if ln else L.rms_norm_bwd_workspace_size
+    ws = torch.empty(max(16, ws_fn(w.rows, w.hidden, host_in["x"].dtype)), dtype=torch.uint8,
                      device=dev)
 
     def one():
-        x.copy_(hx, non_blocking=True)
-        g.copy_(hg, non_blocking=True)
-        dy.copy_(hdy, non_blocking=True)
-        y, rstd = L.rms_norm_fwd(x, g, w.eps, w.offset, w.cast_mode)
-        dx, dw = L.rms_norm_bwd(dy, x, g, rstd, w.offset, workspace=ws)
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        x, g, dy = dev_in["x"], dev_in["gamma"], dev_in["dy"]
+        if ln:
+            y, mean, rstd = L.layer_norm_fwd(x, g, dev_in.get("beta"), w.eps)
+            dx, dgam, dbet = L.layer_norm_bwd(dy, x, g, mean, rstd, with_dbeta=with_beta,
+                                              workspace=ws)
+            outs = [mean, rstd, dgam] + ([dbet] if with_beta else [])
+        else:
+            y, rstd = L.rms_norm_fwd(x, g, w.eps, w.offset, w.cast_mode)
+            dx, dw = L.rms_norm_bwd(dy, x, g, rstd, w.offset, workspace=ws)
+            outs = [rstd, dw]
         hy.copy_(y, non_blocking=True)
-        hr.copy_(rstd, non_blocking=True)
         hdx.copy_(dx, non_blocking=True)
-        hdw.copy_(dw, non_blocking=True)
+        for h, d in zip(stats + grads, outs):
+            h.copy_(d, non_blocking=True)
 
     for _ in range(3):
         one()
@@ -462,8 +511,8 @@ def run_e2e(L, w, inp, dev, steps: int):
         one()
     torch.cuda.synchronize()
     secs = (time.perf_counter() - t) / steps
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hg, hdy))
-    d2h = sum(t.numel() * t.element_size() for t in (hy, hr, hdx, hdw))
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in [hy, hdx] + stats + grads)
     return {"value": round(w.step_bytes() / secs / 1e9, 2), "unit": "GB/s",
             "us_per_step": round(secs * 1e6, 2),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -507,8 +556,7 @@ def load_traffic(workload: str):
 def run_reference(args, rank, world, local):
     if rank != 0:
         return
-    import workloads as W
-    w = W.all_workloads()[args.workload]
+    w = workload_by_name(args.workload)
     # size the sample so that warmup + steps take about two minutes
     probe, _ = time_oracle(w, 64)
     per_row = probe / 64
@@ -527,7 +575,7 @@ def run_reference(args, rank, world, local):
               f"per step (numpy, single thread)")
     line = {
         "impl": "reference",
-        "metric": METRIC,
+        "metric": METRIC_LN if w.kind == "ln" else METRIC,
         "value": round(value, 5),
         "unit": "GB/s",
         "n_gpus": world,

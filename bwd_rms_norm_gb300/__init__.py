@@ -13,6 +13,9 @@ The functions carry the names of the C entry points declared in
 * ``rms_norm_bwd(dy, x, gamma, rstd, offset=0)`` -> ``(dx, dw)``
 * ``rms_norm_bwd_workspace_size(rows, hidden, dtype)``
 * ``rms_norm_status_string(status)``
+* ``rms_norm_bwd_noalloc(dy, x, gamma, rstd, offset=0)`` -> ``(dx, dw)``
+* ``layer_norm_fwd(x, gamma, beta, eps)`` -> ``(y, mean, rstd)``
+* ``layer_norm_bwd(dy, x, gamma, mean, rstd)`` -> ``(dx, dgamma, dbeta)``
 """
 from __future__ import annotations
 
@@ -44,6 +47,9 @@ EXPORTED = (
     "rms_norm_last_launch_count",
     "rms_norm_bwd_noalloc",
     "rms_norm_wait_timeouts",
+    "layer_norm_fwd",
+    "layer_norm_bwd_workspace_size",
+    "layer_norm_bwd",
 )
 
 
@@ -84,6 +90,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_bwd_noalloc.restype = I
     lib.rms_norm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.rms_norm_wait_timeouts.restype = I
+    lib.layer_norm_fwd.argtypes = [P, P, P, P, P, P, I64, I64, F, I, P]
+    lib.layer_norm_fwd.restype = I
+    lib.layer_norm_bwd_workspace_size.argtypes = [I64, I64, I]
+    lib.layer_norm_bwd_workspace_size.restype = SZ
+    lib.layer_norm_bwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I, P, SZ, P]
+    lib.layer_norm_bwd.restype = I
     _lib = lib
     return lib
 
@@ -233,3 +245,70 @@ def rms_norm_bwd_noalloc(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor,
     if st != RMSN_OK:
         raise RMSNormError("rms_norm_bwd_noalloc", st)
     return dx, dw
+
+
+def layer_norm_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Tensor], eps: float,
+                   y: Optional[torch.Tensor] = None, mean: Optional[torch.Tensor] = None,
+                   rstd: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """LayerNorm forward over the last dimension; returns ``(y, mean, rstd)``
+    (``beta`` may be None)."""
+    lib = load_library()
+    _check_cuda("x", x)
+    _check_cuda("gamma", gamma)
+    if beta is not None:
+        _check_cuda("beta", beta)
+        if beta.dtype != x.dtype or beta.numel() != x.shape[-1]:
+            raise RuntimeError("beta must have the dtype of x and hidden elements")
+    if gamma.dtype != x.dtype:
+        raise RuntimeError("gamma must have the dtype of x")
+    rows, hidden = _as_rows(x)
+    if gamma.numel() != hidden:
+        raise RuntimeError("gamma must have hidden elements")
+    y = torch.empty_like(x) if y is None else y
+    mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if mean is None else mean
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
+    with torch.cuda.device(x.device):
+        st = lib.layer_norm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
+                                rows, hidden, float(eps), DTYPE_CODES[x.dtype],
+                                _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("layer_norm_fwd", st)
+    return y, mean, rstd
+
+
+def layer_norm_bwd_workspace_size(rows: int, hidden: int, dtype) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load_library().layer_norm_bwd_workspace_size(int(rows), int(hidden), code))
+
+
+def layer_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor,
+                   rstd: torch.Tensor, dx: Optional[torch.Tensor] = None,
+                   dgamma: Optional[torch.Tensor] = None, dbeta: Optional[torch.Tensor] = None,
+                   with_dbeta: bool = True, workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """LayerNorm backward; returns ``(dx, dgamma, dbeta)`` (dbeta None when
+    ``with_dbeta`` is False)."""
+    lib = load_library()
+    for name, t in (("dy", dy), ("x", x), ("gamma", gamma), ("mean", mean), ("rstd", rstd)):
+        _check_cuda(name, t)
+    if dy.dtype != x.dtype or gamma.dtype != x.dtype:
+        raise RuntimeError("dy, x and gamma must share one dtype")
+    rows, hidden = _as_rows(x)
+    code = DTYPE_CODES[x.dtype]
+    dx = torch.empty_like(x) if dx is None else dx
+    dgamma = torch.empty(hidden, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
+    if with_dbeta and dbeta is None:
+        dbeta = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    need = int(lib.layer_norm_bwd_workspace_size(rows, hidden, code))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(x.device):
+        st = lib.layer_norm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
+                                _ptr(dgamma), _ptr(dbeta) if with_dbeta else None, rows, hidden,
+                                code, workspace.data_ptr(), ws_bytes,
+                                _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("layer_norm_bwd", st)
+    return dx, dgamma, (dbeta if with_dbeta else None)

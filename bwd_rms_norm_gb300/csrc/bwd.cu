@@ -187,36 +187,51 @@ __global__ void __launch_bounds__(256) bwd_scalar(
   }
 }
 
-// dw[j] = sum_b partial[b][j].  Block (32 columns) x (32 lanes over b): lane
-// t sums b = t, t+32, ... in increasing order, then lane 0 adds the 32 lane
-// sums in order.  The order depends only on nparts.
+// out[j] = sum_b partial[b][j] over the `ncols` columns of a [nparts, ncols]
+// fp32 matrix, written to out0[j] for j < split and to out1[j - split]
+// otherwise.  Block (32 columns) x (32 lanes over b): lane t sums b = t,
+// t+32, ... in increasing order, then lane 0 adds the 32 lane sums in order.
+// The order depends only on nparts.
 __global__ void __launch_bounds__(1024) dw_finalize(const float* __restrict__ partial,
-                                                    float* __restrict__ dw, int nparts,
-                                                    int hidden) {
+                                                    int nparts, int ncols,
+                                                    float* __restrict__ out0,
+                                                    float* __restrict__ out1, int split) {
   pdl_trigger();
   pdl_wait();
   __shared__ float s[32][33];
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int j = blockIdx.x * 32 + tx;
   float a = 0.f;
-  if (j < hidden) {
+  if (j < ncols) {
 #pragma unroll 4
-    for (int b = ty; b < nparts; b += 32) a += partial[(int64_t)b * hidden + j];
+    for (int b = ty; b < nparts; b += 32) a += partial[(int64_t)b * ncols + j];
   }
   s[ty][tx] = a;
   __syncthreads();
-  if (ty == 0 && j < hidden) {
+  if (ty == 0 && j < ncols) {
     float t = 0.f;
 #pragma unroll
     for (int q = 0; q < 32; ++q) t += s[q][tx];
-    dw[j] = t;
+    if (j < split)
+      out0[j] = t;
+    else if (out1 != nullptr)
+      out1[j - split] = t;
   }
 }
 
+}  // namespace
+
+cudaError_t launch_column_sums(const float* partial, int nparts, int ncols, float* out0,
+                               float* out1, int split, cudaStream_t s) {
+  return launch_kernel(dw_finalize, dim3((unsigned)((ncols + 31) / 32)), dim3(32, 32), 0, s, 1,
+                       partial, nparts, ncols, out0, out1, split);
+}
+
+namespace {
+
 cudaError_t launch_finalize(const float* partial, float* dw, int nparts, int hidden,
                             cudaStream_t s) {
-  return launch_kernel(dw_finalize, dim3((unsigned)((hidden + 31) / 32)), dim3(32, 32), 0, s, 1,
-                       partial, dw, nparts, hidden);
+  return launch_column_sums(partial, nparts, hidden, dw, nullptr, hidden, s);
 }
 
 template <typename T, int VPT>

@@ -155,6 +155,83 @@ int rms_norm_bwd(const void* dy, const void* x, const void* gamma, const float* 
   return RMSN_OK;
 }
 
+int layer_norm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
+                   float* rstd, int64_t rows, int64_t hidden, float eps, int dtype,
+                   void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
+    return RMSN_ERR_SHAPE;
+  if (!(eps >= 0.f) || isinf(eps)) return RMSN_ERR_EPS;
+  t_last_launches = 0;
+  if (rows == 0) return RMSN_OK;
+  if (!x || !gamma || !y || !mean || !rstd) return RMSN_ERR_NULL;
+  const int s = elem_bytes(dtype);
+  LnFwdArgs a;
+  a.x = x;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.y = y;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.eps = eps;
+  a.vec_ok = ((hidden * s) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y) &&
+             (beta == nullptr || aligned16(beta));
+  int launches = 0;
+  cudaError_t e = launch_ln_fwd(dtype, a, static_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = launches;
+  return RMSN_OK;
+}
+
+size_t layer_norm_bwd_workspace_size(int64_t rows, int64_t hidden, int dtype) {
+  return 2 * rms_norm_bwd_workspace_size(rows, hidden, dtype);
+}
+
+int layer_norm_bwd(const void* dy, const void* x, const void* gamma, const float* mean,
+                   const float* rstd, void* dx, float* dgamma, float* dbeta, int64_t rows,
+                   int64_t hidden, int dtype, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
+    return RMSN_ERR_SHAPE;
+  t_last_launches = 0;
+  if (!dgamma) return RMSN_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {
+    cudaError_t e = cudaMemsetAsync(dgamma, 0, (size_t)hidden * sizeof(float), st);
+    if (e == cudaSuccess && dbeta) e = cudaMemsetAsync(dbeta, 0, (size_t)hidden * sizeof(float), st);
+    return e == cudaSuccess ? RMSN_OK : cuda_fail(e);
+  }
+  if (!dy || !x || !gamma || !mean || !rstd || !dx || !workspace) return RMSN_ERR_NULL;
+  if (!aligned16(workspace)) return RMSN_ERR_ALIGN;
+  if (workspace_bytes < layer_norm_bwd_workspace_size(rows, hidden, dtype))
+    return RMSN_ERR_WORKSPACE;
+  const int s = elem_bytes(dtype);
+  LnBwdArgs a;
+  a.dy = dy;
+  a.x = x;
+  a.gamma = gamma;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.dx = dx;
+  a.dgamma = dgamma;
+  a.dbeta = dbeta;
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.vec_ok = ((hidden * s) % 16 == 0) && aligned16(dy) && aligned16(x) && aligned16(gamma) &&
+             aligned16(dx);
+  a.partial = static_cast<float*>(workspace);
+  a.max_partials = (int64_t)(workspace_bytes / ((size_t)hidden * 2 * sizeof(float)));
+  if (a.max_partials > RMSN_MAX_PARTIALS) a.max_partials = RMSN_MAX_PARTIALS;
+  int launches = 0;
+  cudaError_t e = launch_ln_bwd(dtype, a, st, &launches);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = launches;
+  return RMSN_OK;
+}
+
 const char* rms_norm_status_string(int status) {
   switch (status) {
     case RMSN_OK: return "ok";

@@ -61,6 +61,13 @@ __device__ __forceinline__ void st_vec(void* p, const uint4& v) {
                : "memory");
 }
 
+// Make the compiler forget what it knows about v (no instruction): a value
+// unpacked before and after this point is unpacked twice instead of being
+// held unpacked in registers in between.
+__device__ __forceinline__ void opaque(uint4& v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+}
+
 template <typename T>
 __device__ __forceinline__ void unpack(const uint4& v, float (&f)[Traits<T>::kVec]);
 
@@ -147,6 +154,24 @@ __device__ __forceinline__ float block_sum(float v, float* red, int parity) {
   __syncthreads();
   float s = 0.f;
   for (int w = 0; w < nwarps; ++w) s += slot[w];
+  return s;
+}
+
+// Sum of the pair (a, b) over the whole CTA, same scheme as block_sum;
+// `red` holds 2 x 32 float2.
+__device__ __forceinline__ float2 block_sum2(float a, float b, float2* red, int parity) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  float2* slot = red + 32 * parity;
+  if (lane == 0) slot[warp] = make_float2(a, b);
+  __syncthreads();
+  float2 s = make_float2(0.f, 0.f);
+  for (int w = 0; w < nwarps; ++w) {
+    s.x += slot[w].x;
+    s.y += slot[w].y;
+  }
   return s;
 }
 

@@ -82,6 +82,51 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// out[j] = sum over the nparts rows of the fp32 matrix `partial`
+// [nparts, ncols] in a fixed order; column j goes to out0[j] for j < split,
+// to out1[j - split] otherwise (skipped when out1 is NULL).  bwd.cu.
+cudaError_t launch_column_sums(const float* partial, int nparts, int ncols, float* out0,
+                               float* out1, int split, cudaStream_t s);
+
+// Inputs of one LayerNorm call, already validated (rows >= 1).
+struct LnFwdArgs {
+  const void* x;
+  const void* gamma;
+  const void* beta;   // may be NULL (no bias)
+  void* y;
+  float* mean;
+  float* rstd;
+  int64_t rows;
+  int hidden;
+  float eps;
+  bool vec_ok;
+};
+
+struct LnBwdArgs {
+  const void* dy;
+  const void* x;
+  const void* gamma;
+  const float* mean;
+  const float* rstd;
+  void* dx;
+  float* dgamma;
+  float* dbeta;       // may be NULL (not computed)
+  int64_t rows;
+  int hidden;
+  bool vec_ok;
+  float* partial;     // fp32 workspace, >= max_partials * 2 * hidden floats
+  int64_t max_partials;
+};
+
+cudaError_t launch_ln_fwd(int dtype, const LnFwdArgs& a, cudaStream_t s, int* launches);
+// TMA-staged LayerNorm kernels (tma.cu): false when the row does not fit the
+// pipeline (nothing launched); true with *err set otherwise.  *nparts = the
+// backward's partial rows.
+bool try_launch_ln_fwd_tma(int dtype, const LnFwdArgs& a, cudaStream_t s, cudaError_t* err);
+bool try_launch_ln_bwd_tma(int dtype, const LnBwdArgs& a, cudaStream_t s, cudaError_t* err,
+                           int* nparts);
+cudaError_t launch_ln_bwd(int dtype, const LnBwdArgs& a, cudaStream_t s, int* launches);
+
 // Device properties, cached per device.
 int sm_count(int device);
 int max_blocks_per_sm(const void* func, int block, size_t smem);

@@ -1,5 +1,5 @@
 // Persistent, TMA-staged, warp-specialised forward and backward kernels for
-// sm_103a.
+// sm_103a (RMSNorm, and LayerNorm on the same pipeline).
 //
 // The path is bound by HBM bandwidth.  A row-wise normalisation cannot
 // write any output of a row before the whole row has been reduced, so two
@@ -153,6 +153,7 @@ struct Pipe {
   uint64_t red[kMaxStages];    // a reducer wrote stat[s]
   uint64_t empty[kMaxStages];  // reducer and appliers are done with the stage
   float stat[kMaxStages];      // rstd (forward) or c (backward) of the stage's row
+  float stat2[kMaxStages];     // LayerNorm: mean (forward) or c2 (backward)
   int abort;
 };
 
@@ -492,6 +493,287 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   }
 }
 
+
+// LayerNorm forward.  Reducer: mean, then sum((x - mean)^2) over the row in
+// the stage (two passes over shared memory), rstd; both to global and to
+// the stage's slots.  Appliers: y = round(fma((x - mean) * rstd, gamma,
+// beta)), gains and biases kept packed in registers and widened at use.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kMaxThreads, 1) ln_fwd_tma(
+    const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
+    T* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd, int64_t rows,
+    int hidden, float eps, int stages, int reducers) {
+  constexpr int E = Traits<T>::kVec;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Pipe pipe;
+  const int row_bytes = hidden * (int)sizeof(T);
+  const int stride = (row_bytes + 127) / 128 * 128;
+  const int appliers = blockDim.x - 32 * (1 + reducers);
+  const Rows rw = cta_rows(rows);
+  const int n = rw.n;
+  init_pipe(pipe, stages, appliers / 32);
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  volatile int* abort = &pipe.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = hidden / E;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const void* const src[1] = {x};
+      produce<1>(pipe, smem, stride, stages, src, rw, (uint32_t)row_bytes, abort);
+    }
+    return;
+  }
+
+  if (warp <= reducers) {
+    const int d = warp - 1;
+    RingPos pos{0, 0u};
+    pos.advance(d, stages);
+    for (int i = d; i < n; i += reducers) {
+      if (!__all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort))) return;
+      const uint4* st = reinterpret_cast<const uint4*>(smem + (size_t)pos.stage * stride);
+      float part[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) part[e] = 0.f;
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
+        float f[E];
+        unpack<T>(st[v], f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[e] += f[e];
+      }
+      const float mu = warp_sum(pairwise<E>(part)) / (float)hidden;
+#pragma unroll
+      for (int e = 0; e < E; ++e) part[e] = 0.f;
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
+        float f[E];
+        unpack<T>(st[v], f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float c = f[e] - mu;
+          part[e] = fmaf(c, c, part[e]);
+        }
+      }
+      const float rs = rstd_of(warp_sum(pairwise<E>(part)) / (float)hidden, eps);
+      if (lane == 0) {
+        mean[rw.row(i)] = mu;
+        rstd[rw.row(i)] = rs;
+        pipe.stat[pos.stage] = rs;
+        pipe.stat2[pos.stage] = mu;
+        mbar_arrive(&pipe.red[pos.stage]);
+        mbar_arrive(&pipe.empty[pos.stage]);
+      }
+      pos.advance(reducers, stages);
+    }
+    return;
+  }
+
+  const int a = threadIdx.x - 32 * (1 + reducers);
+  uint4 gp[VPT], bp[VPT];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = a + j * appliers;
+    const bool in = v < nvec;
+    gp[j] = in ? ld_shared_ro(gamma + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+    bp[j] = in && beta ? ld_shared_ro(beta + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+  }
+  RingPos pos{0, 0u};
+  for (int i = 0; i < n; ++i) {
+    bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
+    ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const float rs = pipe.stat[pos.stage], mu = pipe.stat2[pos.stage];
+    const uint4* st = reinterpret_cast<const uint4*>(smem + (size_t)pos.stage * stride);
+    T* yr = y + rw.row(i) * hidden;
+    // widen the packed gains and biases at each use instead of holding them
+    // widened across rows
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      opaque(gp[j]);
+      opaque(bp[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = a + j * appliers;
+      if (v < nvec) {
+        float f[E], g[E], b[E], o[E];
+        unpack<T>(st[v], f);
+        unpack<T>(gp[j], g);
+        unpack<T>(bp[j], b);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = fmaf((f[e] - mu) * rs, g[e], b[e]);
+        st_vec(yr + (int64_t)v * E, pack<T>(o));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
+    pos.advance(1, stages);
+  }
+}
+
+// LayerNorm backward.  Reducer: c1 = sum(g) / hidden and c2 = rstd *
+// sum(g * (x - mean)) / hidden with g = dy * gamma (fp32 gains from the
+// plane-split shared-memory copy).  Appliers: dx = rstd * (g - c1 - x_hat *
+// c2), and fp32 accumulators of dy * x_hat (dgamma) and dy (dbeta) for
+// their columns, written at the end as the CTA's partial row [dgamma | dbeta].
+// Two vectors per applier hold two fp32 accumulator sets of 2E floats each:
+// those blocks are limited to 768 threads, which leaves 80 registers a thread.
+constexpr int kLnBwd2Threads = 768;
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(VPT == 2 ? kLnBwd2Threads : kMaxThreads, 1) ln_bwd_tma(
+    const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
+    const float* __restrict__ mean, const float* __restrict__ rstd, T* __restrict__ dx,
+    float* __restrict__ partial, int64_t rows, int hidden, int stages, int reducers) {
+  constexpr int E = Traits<T>::kVec;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Pipe pipe;
+  const int row_bytes = hidden * (int)sizeof(T);
+  const int stride = (2 * row_bytes + 127) / 128 * 128;
+  const int gain_bytes = (hidden * 4 + 127) / 128 * 128;
+  float* gain = reinterpret_cast<float*>(smem);
+  unsigned char* ring = smem + gain_bytes;
+  const int appliers = blockDim.x - 32 * (1 + reducers);
+  const Rows rw = cta_rows(rows);
+  const int n = rw.n;
+  init_pipe(pipe, stages, appliers / 32);
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  volatile int* abort = &pipe.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = hidden / E;
+  const int doff = row_bytes / 16;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const void* const src[2] = {x, dy};
+      produce<2>(pipe, ring, stride, stages, src, rw, (uint32_t)row_bytes, abort);
+    }
+    return;
+  }
+
+  if (warp <= reducers) {
+    for (int j = threadIdx.x - 32; j < hidden; j += 32 * reducers) {
+      const int v = j / E, e = j % E;
+      gain[((e / 4) * nvec + v) * 4 + (e % 4)] = Traits<T>::to_f(gamma[j]);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * reducers) : "memory");
+    const float4* g4 = reinterpret_cast<const float4*>(gain);
+    const int d = warp - 1;
+    RingPos pos{0, 0u};
+    pos.advance(d, stages);
+    for (int i = d; i < n; i += reducers) {
+      const float mu = __ldg(mean + rw.row(i)), rs = __ldg(rstd + rw.row(i));
+      if (!__all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort))) return;
+      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+      float p1[E], p2[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) p1[e] = p2[e] = 0.f;
+#pragma unroll 2
+      for (int v = lane; v < nvec; v += 32) {
+        float xf[E], df[E], gf[E];
+        unpack<T>(st[v], xf);
+        unpack<T>(st[doff + v], df);
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+          const float4 q = g4[(e / 4) * nvec + v];
+          gf[e] = q.x;
+          gf[e + 1] = q.y;
+          gf[e + 2] = q.z;
+          gf[e + 3] = q.w;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float g = df[e] * gf[e];
+          p1[e] += g;
+          p2[e] = fmaf(g, xf[e] - mu, p2[e]);
+        }
+      }
+      const float s1 = warp_sum(pairwise<E>(p1));
+      const float s2 = warp_sum(pairwise<E>(p2)) * rs;
+      if (lane == 0) {
+        pipe.stat[pos.stage] = s1 / (float)hidden;
+        pipe.stat2[pos.stage] = s2 / (float)hidden;
+        mbar_arrive(&pipe.red[pos.stage]);
+        mbar_arrive(&pipe.empty[pos.stage]);
+      }
+      pos.advance(reducers, stages);
+    }
+    return;
+  }
+
+  const int a = threadIdx.x - 32 * (1 + reducers);
+  uint4 gp[VPT];
+  float ag[VPT][E], ab[VPT][E];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = a + j * appliers;
+    gp[j] = v < nvec ? ld_shared_ro(gamma + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int e = 0; e < E; ++e) ag[j][e] = ab[j][e] = 0.f;
+  }
+  RingPos pos{0, 0u};
+  float mu_next = 0.f, rs_next = 0.f;
+  if (n > 0) {
+    mu_next = __ldg(mean + rw.row(0));
+    rs_next = __ldg(rstd + rw.row(0));
+  }
+  for (int i = 0; i < n; ++i) {
+    const float mu = mu_next, rs = rs_next;
+    if (i + 1 < n) {
+      mu_next = __ldg(mean + rw.row(i + 1));
+      rs_next = __ldg(rstd + rw.row(i + 1));
+    }
+    bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
+    ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const float c1 = pipe.stat[pos.stage], c2 = pipe.stat2[pos.stage];
+    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+    T* dxr = dx + rw.row(i) * hidden;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) opaque(gp[j]);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = a + j * appliers;
+      if (v < nvec) {
+        float xf[E], df[E], gf[E], o[E];
+        unpack<T>(st[v], xf);
+        unpack<T>(st[doff + v], df);
+        unpack<T>(gp[j], gf);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float xh = (xf[e] - mu) * rs;
+          ag[j][e] = fmaf(df[e], xh, ag[j][e]);
+          ab[j][e] += df[e];
+          o[e] = fmaf(-xh, c2, df[e] * gf[e] - c1) * rs;
+        }
+        st_vec(dxr + (int64_t)v * E, pack<T>(o));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
+    pos.advance(1, stages);
+  }
+  float* pr = partial + (int64_t)blockIdx.x * 2 * hidden;
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = a + j * appliers;
+    if (v < nvec) {
+#pragma unroll
+      for (int e = 0; e < E; e += 4) {
+        *reinterpret_cast<float4*>(pr + (int64_t)v * E + e) =
+            make_float4(ag[j][e], ag[j][e + 1], ag[j][e + 2], ag[j][e + 3]);
+        *reinterpret_cast<float4*>(pr + hidden + (int64_t)v * E + e) =
+            make_float4(ab[j][e], ab[j][e + 1], ab[j][e + 2], ab[j][e + 3]);
+      }
+    }
+  }
+}
+
 std::mutex g_attr_mutex;
 struct AttrEntry {
   const void* func;
@@ -626,6 +908,79 @@ bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* npar
   return true;
 }
 
+
+template <typename T, int VPT>
+cudaError_t launch_ln_fwd_tma_v(const LnFwdArgs& a, int appliers, int stages, int reducers,
+                                int grid, cudaStream_t s) {
+  auto kern = ln_fwd_tma<T, VPT>;
+  const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  cudaError_t e = allow_smem((const void*)kern);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, dim3(grid), dim3(32 * (1 + reducers) + appliers),
+                       (size_t)stages * stride, s, 1, static_cast<const T*>(a.x),
+                       static_cast<const T*>(a.gamma), static_cast<const T*>(a.beta),
+                       static_cast<T*>(a.y), a.mean, a.rstd, a.rows, a.hidden, a.eps, stages,
+                       reducers);
+}
+
+template <typename T>
+bool try_ln_fwd_tma_t(const LnFwdArgs& a, cudaStream_t s, cudaError_t* err) {
+  constexpr int E = Traits<T>::kVec;
+  const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  int stages = 0, reducers = 0;
+  split_stages(kRingBudget / stride, &stages, &reducers);
+  if (stages < 3) return false;
+  int appliers = 0;
+  const int vpt = pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 4, &appliers);
+  if (vpt == 0) return false;
+  const int grid = grid_for(a.rows, a.rows, err);
+  if (*err != cudaSuccess) return true;
+  switch (vpt) {
+    case 1: *err = launch_ln_fwd_tma_v<T, 1>(a, appliers, stages, reducers, grid, s); break;
+    case 2: *err = launch_ln_fwd_tma_v<T, 2>(a, appliers, stages, reducers, grid, s); break;
+    default: *err = launch_ln_fwd_tma_v<T, 4>(a, appliers, stages, reducers, grid, s); break;
+  }
+  return true;
+}
+
+template <typename T, int VPT>
+cudaError_t launch_ln_bwd_tma_v(const LnBwdArgs& a, int appliers, int stages, int reducers,
+                                int grid, cudaStream_t s) {
+  auto kern = ln_bwd_tma<T, VPT>;
+  const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
+  cudaError_t e = allow_smem((const void*)kern);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, dim3(grid), dim3(32 * (1 + reducers) + appliers),
+                       (size_t)gain_bytes + (size_t)stages * stride, s, 1,
+                       static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
+                       static_cast<const T*>(a.gamma), a.mean, a.rstd, static_cast<T*>(a.dx),
+                       a.partial, a.rows, a.hidden, stages, reducers);
+}
+
+template <typename T>
+bool try_ln_bwd_tma_t(const LnBwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+  constexpr int E = Traits<T>::kVec;
+  const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
+  int stages = 0, reducers = 0;
+  split_stages((kRingBudget - gain_bytes) / stride, &stages, &reducers);
+  if (stages < 3) return false;
+  int appliers = 0;
+  // at most 2 vectors per applier: two fp32 accumulator sets in registers
+  const int vpt = pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 2, &appliers);
+  if (vpt == 0) return false;
+  if (vpt == 2 && 32 * (1 + reducers) + appliers > kLnBwd2Threads) return false;
+  const int grid = grid_for(a.rows, a.max_partials, err);
+  if (*err != cudaSuccess) return true;
+  *nparts = grid;
+  if (vpt == 1)
+    *err = launch_ln_bwd_tma_v<T, 1>(a, appliers, stages, reducers, grid, s);
+  else
+    *err = launch_ln_bwd_tma_v<T, 2>(a, appliers, stages, reducers, grid, s);
+  return true;
+}
+
 }  // namespace
 
 bool try_launch_fwd_tma(int dtype, const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
@@ -644,6 +999,25 @@ bool try_launch_bwd_tma(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t
     case 0: return try_bwd_tma_t<float>(a, s, err, nparts);
     case 1: return try_bwd_tma_t<__nv_bfloat16>(a, s, err, nparts);
     default: return try_bwd_tma_t<__half>(a, s, err, nparts);
+  }
+}
+
+bool try_launch_ln_fwd_tma(int dtype, const LnFwdArgs& a, cudaStream_t s, cudaError_t* err) {
+  if (!a.vec_ok) return false;
+  switch (dtype) {
+    case 0: return try_ln_fwd_tma_t<float>(a, s, err);
+    case 1: return try_ln_fwd_tma_t<__nv_bfloat16>(a, s, err);
+    default: return try_ln_fwd_tma_t<__half>(a, s, err);
+  }
+}
+
+bool try_launch_ln_bwd_tma(int dtype, const LnBwdArgs& a, cudaStream_t s, cudaError_t* err,
+                           int* nparts) {
+  if (!a.vec_ok) return false;
+  switch (dtype) {
+    case 0: return try_ln_bwd_tma_t<float>(a, s, err, nparts);
+    case 1: return try_ln_bwd_tma_t<__nv_bfloat16>(a, s, err, nparts);
+    default: return try_ln_bwd_tma_t<__half>(a, s, err, nparts);
   }
 }
 

@@ -120,6 +120,38 @@ int rms_norm_bwd(const void* dy, const void* x, const void* gamma,
                  int64_t rows, int64_t hidden, int offset, int dtype,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * LayerNorm, the sibling op: for each row r,
+ *
+ *   mean[r] = (1/hidden) sum_j x[r,j]
+ *   rstd[r] = 1 / sqrt( (1/hidden) sum_j (x[r,j] - mean[r])^2 + eps )
+ *   y[r,j]  = round( (x[r,j] - mean[r]) * rstd[r] * gamma_j + beta_j )
+ *
+ * with fp32 statistics, mean and rstd stored in fp32 (Liger-Kernel PR #1608
+ * "fix(group_norm): keep the backward statistics and reductions in fp32"
+ * notes layer_norm keeps them in fp32) and one rounding at the store.  The
+ * backward (candle PR #4059 adds it with f32 statistics, no formula printed)
+ * is the exact derivative:
+ *
+ *   g = dy * gamma,  c1 = mean_j g,  c2 = mean_j g * x_hat
+ *   dx = rstd * (g - c1 - x_hat * c2);  dgamma = sum_r dy * x_hat;
+ *   dbeta = sum_r dy   (fp32)
+ *
+ * Same conventions, validation and error codes as the RMSNorm entry points.
+ * beta may be NULL (no bias); dbeta may be NULL (not computed).  The
+ * workspace holds min(rows, RMSN_MAX_PARTIALS) partial rows of 2 * hidden
+ * floats.
+ */
+int layer_norm_fwd(const void* x, const void* gamma, const void* beta, void* y,
+                   float* mean, float* rstd, int64_t rows, int64_t hidden,
+                   float eps, int dtype, void* stream);
+size_t layer_norm_bwd_workspace_size(int64_t rows, int64_t hidden, int dtype);
+int layer_norm_bwd(const void* dy, const void* x, const void* gamma,
+                   const float* mean, const float* rstd, void* dx,
+                   float* dgamma, float* dbeta, int64_t rows, int64_t hidden,
+                   int dtype, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* rms_norm_status_string(int status);
 

@@ -12,7 +12,9 @@ within a relative 1e-3.  The readings of these numbers used here:
   rstd * g * eps / (x**2 + eps) -- and fp32 arithmetic cannot resolve an
   element far below the size of the terms it subtracts;
 * for half outputs the same floor applies -- an element passes with at most
-  one ulp OR with |got - ref| <= 1e-5 * s;
+  one ulp OR with |got - ref| <= 1e-5 * s; at most ceil(0.1% of n) of the n
+  compared elements may differ from the reference at all (99.9% identical as
+  a rate, which a sample under 1000 elements cannot show otherwise);
 * round twice rounds x_hat to the storage type, a decision the kernel takes
   on its fp32 x_hat.  Where the exact x_hat lies so close to a rounding
   midpoint that an fp32 x_hat (relative error well under 4e-6) may fall on
@@ -71,7 +73,12 @@ def check_rows(got: np.ndarray, ref: np.ndarray, fmt: str, alt=None, what="y", t
             f"{what}: {bad.shape[0]} elements out of tolerance; first at {i}: "
             f"got {got[i]!r} ref {ref[i]!r}")
     if fmt != "f32":
-        assert same >= MIN_BIT_IDENTICAL, f"{what}: only {same:.5f} bit-identical"
+        # the fraction is a rate: below 1000 compared elements one element
+        # that rounds the other way is already 0.1%, so allow ceil(0.1% n)
+        n = got.size
+        allowed = int(np.ceil((1.0 - MIN_BIT_IDENTICAL) * n - 1e-9))
+        differ = int(round((1.0 - same) * n))
+        assert differ <= allowed, f"{what}: only {same:.5f} bit-identical ({differ} of {n})"
     return {"bit_identical": same, "max_ulp": worst_ulp}
 
 
@@ -88,7 +95,10 @@ def check_dw(got, ref):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     scale = np.maximum(np.abs(ref), np.sqrt(np.mean(ref * ref)))
-    rel = np.abs(got - ref) / scale
+    diff = np.abs(got - ref)
+    # an all-zero reference (a one-element LayerNorm row has x_hat = 0) must
+    # be met exactly
+    rel = np.where(scale > 0, diff / np.where(scale > 0, scale, 1.0), np.where(diff == 0, 0.0, np.inf))
     worst = float(rel.max()) if rel.size else 0.0
     assert worst <= REL_DW, f"dw: worst relative error {worst:.3e}"
     return {"dw_max_rel": worst}

@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rms_norm_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:rms|layer)_norm_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_entry_points():
@@ -123,3 +123,30 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(2, 8)
     with pytest.raises(RuntimeError, match="CUDA"):
         L.rms_norm_fwd(x, torch.ones(8), 1e-5)
+
+
+def test_layer_norm_validation(lib):
+    f = lambda **k: lib.layer_norm_fwd(k.get("x", FAKE), k.get("g", FAKE), k.get("b", NULL),
+                                       k.get("y", FAKE), k.get("m", FAKE), k.get("r", FAKE),
+                                       k.get("rows", 4), k.get("hidden", 64), k.get("eps", 1e-5),
+                                       k.get("dtype", 1), None)
+    assert f(dtype=5) == 4
+    assert f(hidden=0) == 2
+    assert f(eps=-1.0) == 3
+    for k in ("x", "g", "y", "m", "r"):
+        assert f(**{k: NULL}) == 1, k
+    assert f(rows=0, x=NULL, g=NULL, y=NULL, m=NULL, r=NULL) == 0
+    assert lib.layer_norm_bwd_workspace_size(10, 64, 1) == 2 * 10 * 64 * 4
+
+    def b(**k):
+        ws_bytes = k.get("ws_bytes", lib.layer_norm_bwd_workspace_size(4, 64, 1))
+        return lib.layer_norm_bwd(k.get("dy", FAKE), k.get("x", FAKE), k.get("g", FAKE),
+                                  k.get("m", FAKE), k.get("r", FAKE), k.get("dx", FAKE),
+                                  k.get("dg", FAKE), k.get("db", NULL), 4, 64, k.get("dtype", 1),
+                                  k.get("ws", FAKE), ws_bytes, None)
+    assert b(dtype=9) == 4
+    assert b(dg=NULL) == 1
+    for k in ("dy", "x", "g", "m", "r", "dx", "ws"):
+        assert b(**{k: NULL}) == 1, k
+    assert b(ws=ctypes.c_void_p(0x1008)) == 5
+    assert b(ws_bytes=16) == 6

@@ -40,6 +40,8 @@ class Workload:
     gamma_dist: Dist
     dy_dist: Dist
     seed: int = 0
+    kind: str = "rms"                 # "rms" (RMSNorm) or "ln" (LayerNorm)
+    beta_dist: Optional[Dist] = None  # LayerNorm bias; None: no bias
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -49,14 +51,20 @@ class Workload:
         return ELEMENT_BYTES[self.dtype]
 
     def fwd_bytes(self) -> int:
-        """Bytes the forward must move: read x and gamma, write y and rstd."""
+        """Bytes the forward must move: read x and gamma (and beta), write y
+        and the fp32 row statistics (rstd; mean and rstd for LayerNorm)."""
         s, r, n = self.elem_bytes, self.rows, self.hidden
+        if self.kind == "ln":
+            nb = n * s if self.beta_dist is not None else 0
+            return 2 * r * n * s + 8 * r + n * s + nb
         return 2 * r * n * s + 4 * r + n * s
 
     def bwd_bytes(self) -> int:
-        """Bytes the backward must move: read dy, x, gamma and rstd, write dx
-        and the float32 weight gradient."""
+        """Bytes the backward must move: read dy, x, gamma and the statistics,
+        write dx and the fp32 weight (and bias) gradients."""
         s, r, n = self.elem_bytes, self.rows, self.hidden
+        if self.kind == "ln":
+            return 3 * r * n * s + 8 * r + n * s + 8 * n
         return 3 * r * n * s + 4 * r + n * s + 4 * n
 
     def step_bytes(self) -> int:
@@ -100,6 +108,26 @@ def all_workloads() -> Dict[str, Workload]:
     return {w.name: w for w in ws}
 
 
+# LayerNorm cases (the sibling op): x with a nonzero mean so that centring
+# matters, gains near 1, a small bias.
+_LN_X: Dist = ("normal", 0.5, 1.0)
+_LN_BETA: Dist = ("normal", 0.0, 0.01)
+
+
+def layer_norm_workloads() -> Dict[str, Workload]:
+    ws = [
+        Workload("ln_fp32_256x1024", 256, 1024, "f32", 1e-5, 0, "round_once", _LN_X, _U0911,
+                 _N01, kind="ln", beta_dist=_LN_BETA),
+        Workload("ln_bf16_4096x4096", 4096, 4096, "bf16", 1e-5, 0, "round_once", _LN_X, _U0911,
+                 _N01, kind="ln", beta_dist=_LN_BETA),
+        Workload("ln_fp16_4096x8192", 4096, 8192, "f16", 1e-5, 0, "round_once",
+                 ("normal", 2.0, 64.0), _U0911, _N01, kind="ln", beta_dist=_LN_BETA),
+        Workload("ln_bf16_16384x8192", 16384, 8192, "bf16", 1e-5, 0, "round_once", _LN_X,
+                 _U0911, _N01, kind="ln", beta_dist=_LN_BETA),
+    ]
+    return {w.name: w for w in ws}
+
+
 def _draw(shape, dist: Dist, seed: int) -> torch.Tensor:
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
@@ -125,7 +153,10 @@ def make_inputs(w: Workload, rows: Optional[int] = None) -> Dict[str, torch.Tens
     x = _draw((r, w.hidden), w.x_dist, w.seed + 0).to(dt)
     gamma = _draw((w.hidden,), w.gamma_dist, w.seed + 1).to(dt)
     dy = _draw((r, w.hidden), w.dy_dist, w.seed + 2).to(dt)
-    return {"x": x, "gamma": gamma, "dy": dy}
+    out = {"x": x, "gamma": gamma, "dy": dy}
+    if w.beta_dist is not None:
+        out["beta"] = _draw((w.hidden,), w.beta_dist, w.seed + 3).to(dt)
+    return out
 
 
 def as_float64(t: torch.Tensor):
