@@ -22,8 +22,14 @@ Parity status of each function (what pins it is in ``tests/test_oracle.py``):
   float64 and its autograd, finite differences, shift invariance of dx,
   zero mean and the variance identity of x_hat, torch's CPU bf16
   ``layer_norm``.
+* ``fp8.forward_fp8`` / ``store_e4m3`` (and ``rounding.round_to_saturating``)
+  -- pinned in ``tests/test_oracle_fp8.py``: every E4M3 code, every midpoint
+  and the points beside it against torch's float8_e4m3fn cast, the format's
+  value set, torch's float64 ``rms_norm`` times the scale cast by torch, a
+  hand-worked Gemma case; saturation beyond 448 is a reading of the page
+  (torch turns those values into NaN, so nothing outside pins it).
 """
-from . import layer_norm  # noqa: F401
+from . import fp8, layer_norm  # noqa: F401
 from .rounding import FORMATS, max_finite, round_to, ulp_distance  # noqa: F401
 from .rms_norm import (  # noqa: F401
     BF16,

@@ -1,4 +1,4 @@
-"""Round-to-nearest-even from float64 to the three storage formats of the path.
+"""Round-to-nearest-even from float64 to the storage formats of the path.
 
 Test infrastructure only: the oracle is imported by ``tests/``, by the
 ``smoke()`` check in ``__graft_entry__`` and by the CPU-baseline leg of
@@ -9,7 +9,8 @@ The rounding rule is the one "Den dolda avrundningen i RMSNorm"
 helper: round to nearest, ties to even.  That page's helper works on the bit
 pattern of a finite float32 and leaves NaN undefined; this module instead
 rounds a float64 value straight to a format given by its significand width
-and exponent range, so that one routine serves bf16, fp16 and fp32, covers
+and exponent range, so that one routine serves bf16, fp16, fp32 and FP8
+E4M3, covers
 gradual underflow (fp16 subnormals occur in small gradients), overflow to
 infinity, signed zero and NaN, and never rounds twice.
 
@@ -30,13 +31,32 @@ FORMATS = {
     "f32": (24, -126, 127),
     "bf16": (8, -126, 127),
     "f16": (11, -14, 15),
+    # FP8 E4M3 (the "fn" variant: no infinities, and the all-ones code of the
+    # top binade is NaN, so the largest finite value is 1.75 * 2**8 = 448
+    # rather than the 480 of the full grid)
+    "e4m3": (4, -6, 8),
 }
+
+# Formats whose largest finite value is below the top of their grid.
+_MAX_FINITE = {"e4m3": 448.0}
 
 
 def max_finite(fmt: str) -> float:
-    """Largest finite value of ``fmt``: (2 - 2**(1-p)) * 2**emax."""
+    """Largest finite value of ``fmt``: (2 - 2**(1-p)) * 2**emax, except for
+    e4m3, whose top code is NaN (448)."""
+    if fmt in _MAX_FINITE:
+        return _MAX_FINITE[fmt]
     p, _, emax = FORMATS[fmt]
     return float(np.ldexp(2.0 - 2.0 ** (1 - p), emax))
+
+
+def round_to_saturating(v, fmt: str) -> np.ndarray:
+    """``round_to`` followed by clamping to +-max_finite(fmt): a value that
+    rounds past the largest finite value becomes that value with its sign
+    (NaN stays NaN).  The FP8 store of the path converts this way."""
+    r = round_to(v, fmt)
+    m = max_finite(fmt)
+    return np.clip(r, -m, m)
 
 
 def round_to(v, fmt: str) -> np.ndarray:
