@@ -181,10 +181,12 @@ _ORACLE_INPUTS = {}
 
 
 def workload_by_name(name: str):
-    """RMSNorm workloads and the LayerNorm ones (names starting ``ln_``)."""
+    """RMSNorm workloads, the LayerNorm ones (names starting ``ln_``) and the
+    FP8-output ones (names ending ``_fp8``)."""
     import workloads as W
     table = dict(W.all_workloads())
     table.update(W.layer_norm_workloads())
+    table.update(W.fp8_workloads())
     if name not in table:
         raise SystemExit(f"unknown workload {name!r}; known: {', '.join(sorted(table))}")
     return table[name]
@@ -194,6 +196,7 @@ def time_oracle(w, rows: int):
     """Seconds for one oracle forward + backward over ``rows`` rows of ``w``
     (inputs drawn once per row count, outside the timing)."""
     import workloads as W
+    from oracle import fp8 as of8
     from oracle import layer_norm as oln
     from oracle import rms_norm as orm
     ws = w.with_(rows=rows)
@@ -207,6 +210,9 @@ def time_oracle(w, rows: int):
     if ws.kind == "ln":
         _, mean, rstd = oln.forward(xd, gd, bd, ws.eps, ws.dtype)
         oln.backward(dyd, xd, gd, mean, rstd, ws.dtype)
+    elif ws.out_fmt == "e4m3":
+        _, rstd = of8.forward_fp8(xd, gd, ws.eps, ws.offset, ws.scale)
+        orm.backward(dyd, xd, gd, rstd, ws.offset, ws.dtype)
     else:
         _, rstd = orm.forward(xd, gd, ws.eps, ws.offset, ws.dtype, ws.cast_mode)
         orm.backward(dyd, xd, gd, rstd, ws.offset, ws.dtype)
@@ -234,6 +240,7 @@ def run_ours(args, rank, world, local):
     if args.rows:
         w = w.with_(rows=args.rows)
     ln = w.kind == "ln"
+    f8 = w.out_fmt == "e4m3"
     inp = W.make_inputs(w)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
@@ -246,12 +253,14 @@ def run_ours(args, rank, world, local):
     sets = []
     for _ in range(nsets):
         x = inp["x"].to(dev)
-        sets.append({"x": x, "dy": inp["dy"].to(dev), "y": torch.empty_like(x),
+        y = (torch.empty(x.shape, dtype=L.FP8_DTYPE, device=dev) if f8 else torch.empty_like(x))
+        sets.append({"x": x, "dy": inp["dy"].to(dev), "y": y,
                      "dx": torch.empty_like(x),
                      "rstd": torch.empty(w.rows, dtype=torch.float32, device=dev),
                      "mean": torch.empty(w.rows, dtype=torch.float32, device=dev)})
     g = inp["gamma"].to(dev)
     beta = inp["beta"].to(dev) if "beta" in inp else None
+    scale = torch.tensor([w.scale], dtype=torch.float32, device=dev)
     dw = torch.empty(w.hidden, dtype=torch.float32, device=dev)
     db = torch.empty(w.hidden, dtype=torch.float32, device=dev)
     ws_fn = L.layer_norm_bwd_workspace_size if ln else L.rms_norm_bwd_workspace_size
@@ -262,6 +271,8 @@ def run_ours(args, rank, world, local):
         S = sets[k]
         if ln:
             L.layer_norm_fwd(S["x"], g, beta, w.eps, y=S["y"], mean=S["mean"], rstd=S["rstd"])
+        elif f8:
+            L.rms_norm_fwd_fp8(S["x"], g, scale, w.eps, w.offset, y=S["y"], rstd=S["rstd"])
         else:
             L.rms_norm_fwd(S["x"], g, w.eps, w.offset, w.cast_mode, y=S["y"], rstd=S["rstd"])
 
@@ -380,6 +391,7 @@ def run_ours(args, rank, world, local):
                          f"{w.rows} rows ({secs:.1f} s, numpy, single thread)"}
 
     op = "layer_norm" if ln else "rms_norm"
+    fwd_name = f"{op}_fwd" + ("_fp8" if f8 else "")
     line = {
         "metric": METRIC_LN if ln else METRIC,
         "value": round(value, 1),
@@ -398,6 +410,7 @@ def run_ours(args, rank, world, local):
             "rows": w.rows, "hidden": w.hidden, "eps": w.eps,
             **({"bias": beta is not None, "mean": "fp32", "dbeta": "fp32"} if ln else
                {"offset": w.offset, "cast_mode": w.cast_mode}),
+            **({"y": "fp8 e4m3 (saturating)", "scale": w.scale} if f8 else {}),
             "stats": "fp32", "rstd": "fp32", "dw": "fp32", "global_batch_rows": w.rows * world,
             "parallelism": f"replica x{world} (one batch per rank)",
             "l2": (f"inputs larger than L2: {nsets} copies of the batch "
@@ -420,7 +433,7 @@ def run_ours(args, rank, world, local):
             "timing": f"{4 * reps} back-to-back backward calls in a CUDA graph, best of 3",
         },
         "roofline_fwd": {
-            "kernel": f"{op}_fwd", "bound": "hbm", "achieved": round(fwd_ach, 1),
+            "kernel": fwd_name, "bound": "hbm", "achieved": round(fwd_ach, 1),
             "peak": peak, "unit": "GB/s", "frac": round(fwd_ach / peak, 4),
             "traffic": traffic.get("fwd"), "algorithmic_bytes": w.fwd_bytes(),
         },
@@ -473,10 +486,13 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
     copies every result back to pinned host memory."""
     import torch
     ln = w.kind == "ln"
+    f8 = w.out_fmt == "e4m3"
     names = ("x", "gamma", "dy") + (("beta",) if ln and with_beta else ())
     host_in = {k: inp[k].pin_memory() for k in names}
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    hy = torch.empty_like(host_in["x"]).pin_memory()
+    hy = (torch.empty(host_in["x"].shape, dtype=torch.uint8) if f8
+          else torch.empty_like(host_in["x"])).pin_memory()
+    scale = torch.tensor([w.scale], dtype=torch.float32, device=dev)
     hdx = torch.empty_like(host_in["x"]).pin_memory()
     stats = [torch.empty(w.rows, dtype=torch.float32).pin_memory() for _ in range(2 if ln else 1)]
     grads = [torch.empty(w.hidden, dtype=torch.float32).pin_memory()
@@ -494,6 +510,11 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
             dx, dgam, dbet = L.layer_norm_bwd(dy, x, g, mean, rstd, with_dbeta=with_beta,
                                               workspace=ws)
             outs = [mean, rstd, dgam] + ([dbet] if with_beta else [])
+        elif f8:
+            y, rstd = L.rms_norm_fwd_fp8(x, g, scale, w.eps, w.offset)
+            y = y.view(torch.uint8)
+            dx, dw = L.rms_norm_bwd(dy, x, g, rstd, w.offset, workspace=ws)
+            outs = [rstd, dw]
         else:
             y, rstd = L.rms_norm_fwd(x, g, w.eps, w.offset, w.cast_mode)
             dx, dw = L.rms_norm_bwd(dy, x, g, rstd, w.offset, workspace=ws)

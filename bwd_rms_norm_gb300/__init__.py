@@ -14,6 +14,9 @@ The functions carry the names of the C entry points declared in
 * ``rms_norm_bwd_workspace_size(rows, hidden, dtype)``
 * ``rms_norm_status_string(status)``
 * ``rms_norm_bwd_noalloc(dy, x, gamma, rstd, offset=0)`` -> ``(dx, dw)``
+* ``rms_norm_fwd_fp8(x, gamma, scale, eps, offset=0)`` -> ``(y8, rstd)``
+  (``y8`` a torch.float8_e4m3fn tensor, ``scale`` a one-element fp32
+  device tensor)
 * ``layer_norm_fwd(x, gamma, beta, eps)`` -> ``(y, mean, rstd)``
 * ``layer_norm_bwd(dy, x, gamma, mean, rstd)`` -> ``(dx, dgamma, dbeta)``
 """
@@ -47,6 +50,7 @@ EXPORTED = (
     "rms_norm_last_launch_count",
     "rms_norm_bwd_noalloc",
     "rms_norm_wait_timeouts",
+    "rms_norm_fwd_fp8",
     "layer_norm_fwd",
     "layer_norm_bwd_workspace_size",
     "layer_norm_bwd",
@@ -90,6 +94,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_bwd_noalloc.restype = I
     lib.rms_norm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.rms_norm_wait_timeouts.restype = I
+    lib.rms_norm_fwd_fp8.argtypes = [P, P, P, P, P, I64, I64, F, I, I, P]
+    lib.rms_norm_fwd_fp8.restype = I
     lib.layer_norm_fwd.argtypes = [P, P, P, P, P, P, I64, I64, F, I, P]
     lib.layer_norm_fwd.restype = I
     lib.layer_norm_bwd_workspace_size.argtypes = [I64, I64, I]
@@ -176,6 +182,45 @@ def rms_norm_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float, offset: int =
                               CAST_MODES[cast_mode], _stream_handle(x.device, stream))
     if st != RMSN_OK:
         raise RMSNormError("rms_norm_fwd", st)
+    return y, rstd
+
+
+FP8_DTYPE = torch.float8_e4m3fn
+
+
+def rms_norm_fwd_fp8(x: torch.Tensor, gamma: torch.Tensor, scale: torch.Tensor, eps: float,
+                     offset: int = 0, y: Optional[torch.Tensor] = None,
+                     rstd: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None):
+    """Forward with an FP8 E4M3 output: ``y = e4m3(x_hat * gain * scale)``
+    (saturating).  ``scale`` is a one-element fp32 tensor on the device (read
+    by the kernel); returns ``(y, rstd)`` with ``y`` of dtype
+    torch.float8_e4m3fn shaped like ``x``."""
+    lib = load_library()
+    _check_cuda("x", x)
+    _check_cuda("gamma", gamma)
+    _check_cuda("scale", scale)
+    if gamma.dtype != x.dtype:
+        raise RuntimeError("gamma must have the dtype of x")
+    if scale.dtype != torch.float32 or scale.numel() != 1:
+        raise RuntimeError("scale must be a one-element float32 tensor")
+    rows, hidden = _as_rows(x)
+    if gamma.numel() != hidden:
+        raise RuntimeError("gamma must have hidden elements")
+    if y is None:
+        y = torch.empty(x.shape, dtype=FP8_DTYPE, device=x.device)
+    if y.dtype != FP8_DTYPE or y.shape != x.shape:
+        raise RuntimeError("y must be a float8_e4m3fn tensor shaped like x")
+    if rstd is None:
+        rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _check_cuda("y", y)
+    _check_cuda("rstd", rstd)
+    with torch.cuda.device(x.device):
+        st = lib.rms_norm_fwd_fp8(_ptr(x), _ptr(gamma), _ptr(scale), _ptr(y), _ptr(rstd), rows,
+                                  hidden, float(eps), int(offset), DTYPE_CODES[x.dtype],
+                                  _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_fwd_fp8", st)
     return y, rstd
 
 

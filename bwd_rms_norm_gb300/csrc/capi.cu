@@ -99,6 +99,42 @@ int rms_norm_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t
   a.offset = offset;
   a.twice = cast_mode == RMSN_ROUND_TWICE ? 1 : 0;
   a.vec_ok = ((hidden * s) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y);
+  a.fp8 = false;
+  a.scale = nullptr;
+  int launches = 0;
+  cudaError_t e = launch_fwd(dtype, a, static_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = launches;
+  return RMSN_OK;
+}
+
+int rms_norm_fwd_fp8(const void* x, const void* gamma, const float* scale, void* y, float* rstd,
+                     int64_t rows, int64_t hidden, float eps, int offset, int dtype,
+                     void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (offset != 0 && offset != 1) return RMSN_ERR_ARG;
+  if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
+    return RMSN_ERR_SHAPE;
+  if (!(eps >= 0.f) || isinf(eps)) return RMSN_ERR_EPS;
+  t_last_launches = 0;
+  if (rows == 0) return RMSN_OK;
+  if (!x || !gamma || !scale || !y || !rstd) return RMSN_ERR_NULL;
+  const int s = elem_bytes(dtype);
+  FwdArgs a;
+  a.x = x;
+  a.gamma = gamma;
+  a.y = y;
+  a.rstd = rstd;
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.eps = eps;
+  a.offset = offset;
+  a.twice = 0;
+  // a 16-byte input vector becomes 16/s output bytes: rows of y start on
+  // that boundary when y does
+  a.vec_ok = ((hidden * s) % 16 == 0) && aligned16(x) && aligned16(gamma) && aligned16(y);
+  a.fp8 = true;
+  a.scale = scale;
   int launches = 0;
   cudaError_t e = launch_fwd(dtype, a, static_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return cuda_fail(e);

@@ -61,6 +61,38 @@ __device__ __forceinline__ void st_vec(void* p, const uint4& v) {
                : "memory");
 }
 
+// fp32 to FP8 E4M3 (the fn variant): round to nearest even, saturating to
+// +-448, NaN kept.  The hardware conversion packs two values: the second
+// source operand goes to the low byte, so passing (b, a) puts a at the lower
+// address.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  unsigned short lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ unsigned char e4m3(float a) {
+  unsigned short v;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(0.f), "f"(a));
+  return (unsigned char)(v & 0xff);
+}
+
+// E FP8 values (one 16-byte input vector's worth) to p: 8 bytes for a
+// half-precision input, 4 for fp32; p is aligned to that size.
+template <int E>
+__device__ __forceinline__ void st_e4m3(void* p, const float (&o)[E]) {
+  if constexpr (E == 8) {
+    const uint32_t u = e4m3x4(o[0], o[1], o[2], o[3]);
+    const uint32_t w = e4m3x4(o[4], o[5], o[6], o[7]);
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(u), "r"(w) : "memory");
+  } else {
+    static_assert(E == 4, "E4M3 store of 4 or 8 values");
+    const uint32_t u = e4m3x4(o[0], o[1], o[2], o[3]);
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(u) : "memory");
+  }
+}
+
 // Make the compiler forget what it knows about v (no instruction): a value
 // unpacked before and after this point is unpacked twice instead of being
 // held unpacked in registers in between.

@@ -4,7 +4,10 @@
 // fp32, then y = round(x * rstd * gain) with a single rounding (round once)
 // or y = round(round(x * rstd) * gain) (round twice) -- "Den dolda
 // avrundningen i RMSNorm", sections "En välbekant operation" and "Två
-// ställen att avrunda"; statistics in fp32 as in Liger-Kernel PR #92.
+// ställen att avrunda"; statistics in fp32 as in Liger-Kernel PR #92.  The
+// FP8 variant (template flag F8) stores E4M3 of ((x * rstd) * gain) * scale,
+// every step in fp32 and one conversion at the end (same page, section "Var
+// implementationerna skiljer sig", the Transformer Engine paragraph).
 //
 // The path is bound by HBM bandwidth: each element is read once and written
 // once, so the row stays in registers between the reduction and the store.
@@ -37,11 +40,30 @@ __device__ __forceinline__ uint4 scale_vec(const float (&xf)[Traits<T>::kVec],
   return pack<T>(o);
 }
 
-template <typename T, int VPT>
+// Store one vector of outputs at element `elem` of y: the storage type T, or
+// FP8 E4M3 of ((x * rstd) * gain) * scale, every step in fp32 and a single
+// conversion at the end.
+template <typename T, bool F8>
+__device__ __forceinline__ void store_vec(void* y, int64_t elem,
+                                          const float (&xf)[Traits<T>::kVec], const uint4& gv,
+                                          float rs, float off, int twice, float sc) {
+  constexpr int E = Traits<T>::kVec;
+  if constexpr (F8) {
+    float gf[E], o[E];
+    unpack<T>(gv, gf);
+#pragma unroll
+    for (int i = 0; i < E; ++i) o[i] = ((xf[i] * rs) * (gf[i] + off)) * sc;
+    st_e4m3<E>(static_cast<unsigned char*>(y) + elem, o);
+  } else {
+    st_vec(static_cast<T*>(y) + elem, scale_vec<T>(xf, gv, rs, off, twice));
+  }
+}
+
+template <typename T, int VPT, bool F8>
 __global__ void __launch_bounds__(256) fwd_warp_rows(
-    const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+    const T* __restrict__ x, const T* __restrict__ gamma, void* __restrict__ y,
     float* __restrict__ rstd, int64_t rows, int hidden, float eps, float off,
-    int twice) {
+    int twice, const float* __restrict__ scale) {
   constexpr int E = Traits<T>::kVec;
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -50,7 +72,7 @@ __global__ void __launch_bounds__(256) fwd_warp_rows(
   pdl_wait();
   const int nvec = hidden / E;
   const T* xr = x + row * hidden;
-  T* yr = y + row * hidden;
+  const float sc = F8 ? __ldg(scale) : 1.f;
 
   uint4 xv[VPT];
 #pragma unroll
@@ -76,23 +98,24 @@ __global__ void __launch_bounds__(256) fwd_warp_rows(
       float f[E];
       unpack<T>(xv[k], f);
       const uint4 gv = ld_shared_ro(gamma + (int64_t)v * E);
-      st_vec(yr + (int64_t)v * E, scale_vec<T>(f, gv, rs, off, twice));
+      store_vec<T, F8>(y, row * hidden + (int64_t)v * E, f, gv, rs, off, twice, sc);
     }
   }
 }
 
-template <typename T, int VPT>
+template <typename T, int VPT, bool F8>
 __global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) fwd_cta_row(
-    const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
-    float* __restrict__ rstd, int hidden, float eps, float off, int twice) {
+    const T* __restrict__ x, const T* __restrict__ gamma, void* __restrict__ y,
+    float* __restrict__ rstd, int hidden, float eps, float off, int twice,
+    const float* __restrict__ scale) {
   constexpr int E = Traits<T>::kVec;
   __shared__ float red[64];
   const int64_t row = blockIdx.x;
   const int nvec = hidden / E;
   const T* xr = x + row * hidden;
-  T* yr = y + row * hidden;
   pdl_trigger();
   pdl_wait();
+  const float sc = F8 ? __ldg(scale) : 1.f;
 
   uint4 xv[VPT];
 #pragma unroll
@@ -118,21 +141,22 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) fwd_cta_row(
       float f[E];
       unpack<T>(xv[k], f);
       const uint4 gv = ld_shared_ro(gamma + (int64_t)v * E);
-      st_vec(yr + (int64_t)v * E, scale_vec<T>(f, gv, rs, off, twice));
+      store_vec<T, F8>(y, row * hidden + (int64_t)v * E, f, gv, rs, off, twice, sc);
     }
   }
 }
 
-template <typename T>
+template <typename T, bool F8>
 __global__ void __launch_bounds__(256) fwd_scalar(
-    const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
-    float* __restrict__ rstd, int hidden, float eps, float off, int twice) {
+    const T* __restrict__ x, const T* __restrict__ gamma, void* __restrict__ y,
+    float* __restrict__ rstd, int hidden, float eps, float off, int twice,
+    const float* __restrict__ scale) {
   __shared__ float red[64];
   const int64_t row = blockIdx.x;
   const T* xr = x + row * hidden;
-  T* yr = y + row * hidden;
   pdl_trigger();
   pdl_wait();
+  const float sc = F8 ? __ldg(scale) : 1.f;
   float ss = 0.f;
   for (int j = threadIdx.x; j < hidden; j += blockDim.x) {
     const float f = Traits<T>::to_f(xr[j]);
@@ -144,8 +168,12 @@ __global__ void __launch_bounds__(256) fwd_scalar(
   for (int j = threadIdx.x; j < hidden; j += blockDim.x) {
     const float xh = Traits<T>::to_f(xr[j]) * rs;
     const float g = Traits<T>::to_f(gamma[j]) + off;
-    const float o = twice ? round_trip<T>(xh) * g : xh * g;
-    yr[j] = Traits<T>::from_f(o);
+    if constexpr (F8) {
+      static_cast<unsigned char*>(y)[row * hidden + j] = e4m3((xh * g) * sc);
+    } else {
+      const float o = twice ? round_trip<T>(xh) * g : xh * g;
+      static_cast<T*>(y)[row * hidden + j] = Traits<T>::from_f(o);
+    }
   }
 }
 
@@ -163,26 +191,27 @@ int pow2_at_least(int v) {
 // Rows of up to this many 16-byte vectors run one warp per row.
 constexpr int kWarpRowMaxVec = 128;
 
-template <typename T>
+template <typename T, bool F8>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
   constexpr int E = Traits<T>::kVec;
   const T* x = static_cast<const T*>(a.x);
   const T* g = static_cast<const T*>(a.gamma);
-  T* y = static_cast<T*>(a.y);
+  void* y = a.y;
   const float off = a.offset ? 1.f : 0.f;
   const int nvec = a.hidden / E;
+  const float* sc = a.scale;
   cudaError_t e = cudaSuccess;
 
   if (a.vec_ok && nvec <= kWarpRowMaxVec) {
     // one warp per row, 8 rows per CTA
     const int vpt = pow2_at_least((nvec + 31) / 32);
-    const int64_t grid = (a.rows + 7) / 8;
+    const dim3 grid((unsigned)((a.rows + 7) / 8));
     switch (vpt) {
-      case 1: e = launch_kernel(fwd_warp_rows<T, 1>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
-      case 2: e = launch_kernel(fwd_warp_rows<T, 2>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
-      case 4: e = launch_kernel(fwd_warp_rows<T, 4>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
-      case 8: e = launch_kernel(fwd_warp_rows<T, 8>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
-      default: e = launch_kernel(fwd_warp_rows<T, 16>, dim3((unsigned)grid), dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice); break;
+      case 1: e = launch_kernel(fwd_warp_rows<T, 1, F8>, grid, dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice, sc); break;
+      case 2: e = launch_kernel(fwd_warp_rows<T, 2, F8>, grid, dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice, sc); break;
+      case 4: e = launch_kernel(fwd_warp_rows<T, 4, F8>, grid, dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice, sc); break;
+      case 8: e = launch_kernel(fwd_warp_rows<T, 8, F8>, grid, dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice, sc); break;
+      default: e = launch_kernel(fwd_warp_rows<T, 16, F8>, grid, dim3(256), 0, s, 1, x, g, y, a.rstd, a.rows, a.hidden, a.eps, off, a.twice, sc); break;
     }
     if (e == cudaSuccess) *launches += 1;
     return e;
@@ -198,24 +227,26 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
     if (vpt > 16) vpt = 16;
     const int tpr = ((nvec + vpt - 1) / vpt + 31) / 32 * 32;
     if (tpr <= (vpt >= 8 ? 512 : 1024)) {
-      const unsigned grid = (unsigned)a.rows;
+      const dim3 grid((unsigned)a.rows);
       switch (vpt) {
-        case 1: e = launch_kernel(fwd_cta_row<T, 1>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
-        case 2: e = launch_kernel(fwd_cta_row<T, 2>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
-        case 4: e = launch_kernel(fwd_cta_row<T, 4>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
-        case 8: e = launch_kernel(fwd_cta_row<T, 8>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
-        default: e = launch_kernel(fwd_cta_row<T, 16>, dim3(grid), dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice); break;
+        case 1: e = launch_kernel(fwd_cta_row<T, 1, F8>, grid, dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice, sc); break;
+        case 2: e = launch_kernel(fwd_cta_row<T, 2, F8>, grid, dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice, sc); break;
+        case 4: e = launch_kernel(fwd_cta_row<T, 4, F8>, grid, dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice, sc); break;
+        case 8: e = launch_kernel(fwd_cta_row<T, 8, F8>, grid, dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice, sc); break;
+        default: e = launch_kernel(fwd_cta_row<T, 16, F8>, grid, dim3(tpr), 0, s, 1, x, g, y, a.rstd, a.hidden, a.eps, off, a.twice, sc); break;
       }
       if (e == cudaSuccess) *launches += 1;
       return e;
     }
   }
-  if (try_launch_fwd_cluster(dtype_code<T>(), a, s, &e)) {
+  // the cluster kernels store the storage type only; an FP8 row this wide
+  // takes the scalar kernel
+  if (!F8 && try_launch_fwd_cluster(dtype_code<T>(), a, s, &e)) {
     if (e == cudaSuccess) *launches += 1;
     return e;
   }
-  e = launch_kernel(fwd_scalar<T>, dim3((unsigned)a.rows), dim3(256), 0, s, 1, x, g, y, a.rstd,
-                    a.hidden, a.eps, off, a.twice);
+  e = launch_kernel(fwd_scalar<T, F8>, dim3((unsigned)a.rows), dim3(256), 0, s, 1, x, g, y,
+                    a.rstd, a.hidden, a.eps, off, a.twice, sc);
   if (e == cudaSuccess) *launches += 1;
   return e;
 }
@@ -234,10 +265,17 @@ cudaError_t launch_fwd(int dtype, const FwdArgs& a, cudaStream_t s, int* launche
     if (e == cudaSuccess) *launches += 1;
     return e;
   }
+  if (a.fp8) {
+    switch (dtype) {
+      case 0: return launch_fwd_t<float, true>(a, s, launches);
+      case 1: return launch_fwd_t<__nv_bfloat16, true>(a, s, launches);
+      default: return launch_fwd_t<__half, true>(a, s, launches);
+    }
+  }
   switch (dtype) {
-    case 0: return launch_fwd_t<float>(a, s, launches);
-    case 1: return launch_fwd_t<__nv_bfloat16>(a, s, launches);
-    default: return launch_fwd_t<__half>(a, s, launches);
+    case 0: return launch_fwd_t<float, false>(a, s, launches);
+    case 1: return launch_fwd_t<__nv_bfloat16, false>(a, s, launches);
+    default: return launch_fwd_t<__half, false>(a, s, launches);
   }
 }
 

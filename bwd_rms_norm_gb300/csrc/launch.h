@@ -20,6 +20,8 @@ struct FwdArgs {
   int offset;      // 0: gain gamma, 1: gain 1 + gamma
   int twice;       // 1: round x_hat to the storage type before the gain
   bool vec_ok;     // 16-byte aligned rows: the vector kernels may run
+  bool fp8;        // y is FP8 E4M3 of x_hat * gain * (*scale)
+  const float* scale;  // device pointer (fp8 only)
 };
 
 // Inputs of one backward call, already validated (rows >= 1).

@@ -247,11 +247,11 @@ __device__ __forceinline__ float pairwise(float (&p)[E]) {
 // Forward.  Reducer: sum of squares of its row, rstd, written to global and
 // to the stage's slot.  Appliers: y = round((x * rstd) * gain) (or the
 // round-twice store) for their vectors of every row.
-template <typename T, int VPT>
+template <typename T, int VPT, bool F8>
 __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
-    const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+    const T* __restrict__ x, const T* __restrict__ gamma, void* __restrict__ y,
     float* __restrict__ rstd, int64_t rows, int hidden, float eps, float off, int twice,
-    int stages, int reducers) {
+    const float* __restrict__ scale, int stages, int reducers) {
   constexpr int E = Traits<T>::kVec;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Pipe pipe;
@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
   }
 
   const int a = threadIdx.x - 32 * (1 + reducers);
+  const float sc = F8 ? __ldg(scale) : 1.f;
   float ge[VPT][E];
 #pragma unroll
   for (int j = 0; j < VPT; ++j) {
@@ -324,13 +325,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
     if (!__all_sync(0xffffffffu, ok)) return;
     const float rs = pipe.stat[pos.stage];
     const uint4* st = reinterpret_cast<const uint4*>(smem + (size_t)pos.stage * stride);
-    T* yr = y + rw.row(i) * hidden;
+    T* yr = static_cast<T*>(y) + rw.row(i) * hidden;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
       const int v = a + j * appliers;
       if (v < nvec) {
         float f[E], o[E];
         unpack<T>(st[v], f);
+        if constexpr (F8) {
+          // ((x * rstd) * gain) * scale in fp32, one conversion to E4M3
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[e] = ((f[e] * rs) * ge[j][e]) * sc;
+          st_e4m3<E>(static_cast<unsigned char*>(y) + rw.row(i) * hidden + (int64_t)v * E, o);
+          continue;
+        }
         if (twice) {
 #pragma unroll
           for (int e = 0; e < E; ++e) o[e] = round_trip<T>(f[e] * rs) * ge[j][e];
@@ -837,17 +845,24 @@ int grid_for(int64_t rows, int64_t cap, cudaError_t* err) {
   return (int)g;
 }
 
-template <typename T, int VPT>
-cudaError_t launch_fwd_tma_v(const FwdArgs& a, int appliers, int stages, int reducers, int grid,
-                             cudaStream_t s) {
-  auto kern = fwd_tma<T, VPT>;
+template <typename T, int VPT, bool F8>
+cudaError_t launch_fwd_tma_vf(const FwdArgs& a, int appliers, int stages, int reducers, int grid,
+                              cudaStream_t s) {
+  auto kern = fwd_tma<T, VPT, F8>;
   const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   cudaError_t e = allow_smem((const void*)kern);
   if (e != cudaSuccess) return e;
   return launch_kernel(kern, dim3(grid), dim3(32 * (1 + reducers) + appliers),
                        (size_t)stages * stride, s, 1, static_cast<const T*>(a.x),
-                       static_cast<const T*>(a.gamma), static_cast<T*>(a.y), a.rstd, a.rows,
-                       a.hidden, a.eps, a.offset ? 1.f : 0.f, a.twice, stages, reducers);
+                       static_cast<const T*>(a.gamma), a.y, a.rstd, a.rows, a.hidden, a.eps,
+                       a.offset ? 1.f : 0.f, a.twice, a.scale, stages, reducers);
+}
+
+template <typename T, int VPT>
+cudaError_t launch_fwd_tma_v(const FwdArgs& a, int appliers, int stages, int reducers, int grid,
+                             cudaStream_t s) {
+  return a.fp8 ? launch_fwd_tma_vf<T, VPT, true>(a, appliers, stages, reducers, grid, s)
+               : launch_fwd_tma_vf<T, VPT, false>(a, appliers, stages, reducers, grid, s);
 }
 
 template <typename T>

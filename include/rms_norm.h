@@ -121,6 +121,37 @@ int rms_norm_bwd(const void* dy, const void* x, const void* gamma,
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * RMSNorm forward with an FP8 output and a per-tensor scale ("Den dolda
+ * avrundningen i RMSNorm", section "Var implementationerna skiljer sig", the
+ * Transformer Engine paragraph and footnote 3): the normalisation, the gain
+ * and the output scale are applied in fp32 and only the final conversion to
+ * FP8 rounds:
+ *
+ *   rstd[r] = 1 / sqrt( (1/hidden) sum_j x[r,j]^2 + eps )        (fp32)
+ *   y[r,j]  = e4m3( ((x[r,j] * rstd[r]) * gain_j) * scale )
+ *
+ * gain_j = gamma_j (offset 0) or 1 + gamma_j (offset 1).  e4m3 is FP8 E4M3
+ * (the "fn" variant: 1 sign, 4 exponent, 3 mantissa bits, no infinities,
+ * largest finite value 448), rounding to nearest even and SATURATING: a
+ * value beyond +-448 is stored as +-448; NaN stays NaN.
+ *
+ *   x, gamma  device, dtype (fp32/bf16/fp16), as rms_norm_fwd
+ *   scale     device pointer to ONE fp32 value, read by the kernel (so a
+ *             captured CUDA graph sees updates to it)
+ *   y         device, rows x hidden bytes (E4M3 codes), row-major
+ *   rstd      device, rows fp32 -- the same rstd as rms_norm_fwd, so
+ *             rms_norm_bwd runs unchanged on (dy, x, gamma, rstd)
+ *
+ * There is no round-twice mode here.  Vector kernels run when x, gamma and
+ * y are 16-byte aligned and hidden * sizeof(dtype) is a multiple of 16;
+ * otherwise a scalar kernel.  Validation and error codes as rms_norm_fwd
+ * (scale NULL with rows > 0: RMSN_ERR_NULL).
+ */
+int rms_norm_fwd_fp8(const void* x, const void* gamma, const float* scale,
+                     void* y, float* rstd, int64_t rows, int64_t hidden,
+                     float eps, int offset, int dtype, void* stream);
+
+/*
  * LayerNorm, the sibling op: for each row r,
  *
  *   mean[r] = (1/hidden) sum_j x[r,j]

@@ -150,3 +150,20 @@ def test_layer_norm_validation(lib):
         assert b(**{k: NULL}) == 1, k
     assert b(ws=ctypes.c_void_p(0x1008)) == 5
     assert b(ws_bytes=16) == 6
+
+
+def test_fp8_forward_validation(lib):
+    """Host-side checks of rms_norm_fwd_fp8 (no kernel runs: every case is
+    rejected before a launch, or has rows == 0)."""
+    def f(**k):
+        return lib.rms_norm_fwd_fp8(k.get("x", FAKE), k.get("g", FAKE), k.get("s", FAKE),
+                                    k.get("y", FAKE), k.get("r", FAKE), k.get("rows", 4),
+                                    k.get("hidden", 64), k.get("eps", 1e-5), k.get("offset", 0),
+                                    k.get("dtype", 1), None)
+    assert f(dtype=3) == 4
+    assert f(offset=2) == 8
+    assert f(hidden=0) == 2 and f(hidden=65537) == 2 and f(rows=-1) == 2
+    assert f(eps=float("nan")) == 3 and f(eps=float("inf")) == 3
+    for k in ("x", "g", "s", "y", "r"):
+        assert f(**{k: NULL}) == 1, k
+    assert f(rows=0, x=NULL, g=NULL, s=NULL, y=NULL, r=NULL) == 0

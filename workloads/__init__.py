@@ -42,6 +42,8 @@ class Workload:
     seed: int = 0
     kind: str = "rms"                 # "rms" (RMSNorm) or "ln" (LayerNorm)
     beta_dist: Optional[Dist] = None  # LayerNorm bias; None: no bias
+    out_fmt: Optional[str] = None     # "e4m3": FP8 forward output (RMSNorm)
+    scale: float = 1.0                # per-tensor scale of the FP8 output
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -57,6 +59,9 @@ class Workload:
         if self.kind == "ln":
             nb = n * s if self.beta_dist is not None else 0
             return 2 * r * n * s + 8 * r + n * s + nb
+        if self.out_fmt == "e4m3":
+            # read x, write one byte per element, rstd, gamma, the scale
+            return r * n * s + r * n + 4 * r + n * s + 4
         return 2 * r * n * s + 4 * r + n * s
 
     def bwd_bytes(self) -> int:
@@ -105,6 +110,16 @@ def all_workloads() -> Dict[str, Workload]:
     ws = [FP32_256x1024, LLAMA_BF16_4096x4096, GEMMA_BF16_8192x3072]
     ws += [fp16_sweep(n) for n in FP16_SWEEP_HIDDEN]
     ws += [large_bf16("round_once"), large_bf16("round_twice")]
+    return {w.name: w for w in ws}
+
+
+def fp8_workloads() -> Dict[str, Workload]:
+    """The bf16 RMSNorm workloads with an FP8 E4M3 forward output, scale 32
+    (|x_hat * gamma| stays below 448 / 32 for these draws except far in the
+    tail, where the store saturates)."""
+    ws = [LLAMA_BF16_4096x4096.with_(name="llama_bf16_4096x4096_fp8", out_fmt="e4m3", scale=32.0),
+          large_bf16("round_once").with_(name="large_bf16_16384x8192_fp8", out_fmt="e4m3",
+                                         scale=32.0)]
     return {w.name: w for w in ws}
 
 
