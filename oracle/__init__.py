@@ -28,8 +28,13 @@ Parity status of each function (what pins it is in ``tests/test_oracle.py``):
   value set, torch's float64 ``rms_norm`` times the scale cast by torch, a
   hand-worked Gemma case; saturation beyond 448 is a reading of the page
   (torch turns those values into NaN, so nothing outside pins it).
+* ``softmax.forward`` / ``backward`` (and the ``_exact`` forms) -- pinned in
+  ``tests/test_oracle_softmax.py``: torch's CPU softmax in float64 (with a
+  row whose exp overflows unshifted) and its autograd, finite differences,
+  rows summing to 1, dx rows summing to 0, shift invariance, closed forms
+  for one, two and constant elements, torch's CPU bf16 softmax.
 """
-from . import fp8, layer_norm  # noqa: F401
+from . import fp8, layer_norm, softmax  # noqa: F401
 from .rounding import FORMATS, max_finite, round_to, ulp_distance  # noqa: F401
 from .rms_norm import (  # noqa: F401
     BF16,
