@@ -50,6 +50,11 @@ if ROOT not in sys.path:
 
 METRIC = "RMSNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
 METRIC_LN = "LayerNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
+METRIC_SM = "Softmax (last dim) fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
+
+
+def metric_for(w) -> str:
+    return {"ln": METRIC_LN, "softmax": METRIC_SM}.get(w.kind, METRIC)
 DEFAULT_WORKLOAD = "llama_bf16_4096x4096"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -181,12 +186,14 @@ _ORACLE_INPUTS = {}
 
 
 def workload_by_name(name: str):
-    """RMSNorm workloads, the LayerNorm ones (names starting ``ln_``) and the
-    FP8-output ones (names ending ``_fp8``)."""
+    """RMSNorm workloads, the LayerNorm ones (names starting ``ln_``), the
+    FP8-output ones (names ending ``_fp8``) and the softmax ones (names
+    starting ``softmax_``)."""
     import workloads as W
     table = dict(W.all_workloads())
     table.update(W.layer_norm_workloads())
     table.update(W.fp8_workloads())
+    table.update(W.softmax_workloads())
     if name not in table:
         raise SystemExit(f"unknown workload {name!r}; known: {', '.join(sorted(table))}")
     return table[name]
@@ -199,6 +206,7 @@ def time_oracle(w, rows: int):
     from oracle import fp8 as of8
     from oracle import layer_norm as oln
     from oracle import rms_norm as orm
+    from oracle import softmax as osm
     ws = w.with_(rows=rows)
     if (ws.name, rows) not in _ORACLE_INPUTS:
         _ORACLE_INPUTS.clear()
@@ -207,7 +215,10 @@ def time_oracle(w, rows: int):
             W.as_float64(inp[k]) if k in inp else None for k in ("x", "gamma", "dy", "beta"))
     xd, gd, dyd, bd = _ORACLE_INPUTS[(ws.name, rows)]
     t = time.perf_counter()
-    if ws.kind == "ln":
+    if ws.kind == "softmax":
+        y = osm.forward(xd, ws.dtype)
+        osm.backward(dyd, y, ws.dtype)
+    elif ws.kind == "ln":
         _, mean, rstd = oln.forward(xd, gd, bd, ws.eps, ws.dtype)
         oln.backward(dyd, xd, gd, mean, rstd, ws.dtype)
     elif ws.out_fmt == "e4m3":
@@ -240,6 +251,7 @@ def run_ours(args, rank, world, local):
     if args.rows:
         w = w.with_(rows=args.rows)
     ln = w.kind == "ln"
+    sm = w.kind == "softmax"
     f8 = w.out_fmt == "e4m3"
     inp = W.make_inputs(w)
     props = torch.cuda.get_device_properties(dev)
@@ -269,7 +281,9 @@ def run_ours(args, rank, world, local):
 
     def fwd(k):
         S = sets[k]
-        if ln:
+        if sm:
+            L.softmax_fwd(S["x"], y=S["y"])
+        elif ln:
             L.layer_norm_fwd(S["x"], g, beta, w.eps, y=S["y"], mean=S["mean"], rstd=S["rstd"])
         elif f8:
             L.rms_norm_fwd_fp8(S["x"], g, scale, w.eps, w.offset, y=S["y"], rstd=S["rstd"])
@@ -278,7 +292,9 @@ def run_ours(args, rank, world, local):
 
     def bwd(k):
         S = sets[k]
-        if ln:
+        if sm:
+            L.softmax_bwd(S["dy"], S["y"], dx=S["dx"])
+        elif ln:
             L.layer_norm_bwd(S["dy"], S["x"], g, S["mean"], S["rstd"], dx=S["dx"], dgamma=dw,
                              dbeta=db, workspace=ws)
         else:
@@ -390,10 +406,10 @@ def run_ours(args, rank, world, local):
                "sample": f"{args.workload}: {passes} float64 forward+backward passes over all "
                          f"{w.rows} rows ({secs:.1f} s, numpy, single thread)"}
 
-    op = "layer_norm" if ln else "rms_norm"
+    op = "layer_norm" if ln else "softmax" if sm else "rms_norm"
     fwd_name = f"{op}_fwd" + ("_fp8" if f8 else "")
     line = {
-        "metric": METRIC_LN if ln else METRIC,
+        "metric": metric_for(w),
         "value": round(value, 1),
         "unit": "GB/s",
         "n_gpus": world,
@@ -407,11 +423,13 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded, see workloads/)",
         "config": {
             "workload": args.workload + (f" (rows overridden to {w.rows})" if args.rows else ""),
-            "rows": w.rows, "hidden": w.hidden, "eps": w.eps,
-            **({"bias": beta is not None, "mean": "fp32", "dbeta": "fp32"} if ln else
-               {"offset": w.offset, "cast_mode": w.cast_mode}),
+            "rows": w.rows, "hidden": w.hidden,
+            **({"arith": "fp32 exp/sum/dot, one rounding at each store"} if sm else
+               {"eps": w.eps, "stats": "fp32", "rstd": "fp32", "dw": "fp32"}),
+            **({"bias": beta is not None, "mean": "fp32", "dbeta": "fp32"} if ln else {}),
+            **({"offset": w.offset, "cast_mode": w.cast_mode} if not (ln or sm) else {}),
             **({"y": "fp8 e4m3 (saturating)", "scale": w.scale} if f8 else {}),
-            "stats": "fp32", "rstd": "fp32", "dw": "fp32", "global_batch_rows": w.rows * world,
+            "global_batch_rows": w.rows * world,
             "parallelism": f"replica x{world} (one batch per rank)",
             "l2": (f"inputs larger than L2: {nsets} copies of the batch "
                    f"({nsets * set_bytes / 2**20:.0f} MiB) cycled; each step's backward "
@@ -486,17 +504,19 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
     copies every result back to pinned host memory."""
     import torch
     ln = w.kind == "ln"
+    sm = w.kind == "softmax"
     f8 = w.out_fmt == "e4m3"
-    names = ("x", "gamma", "dy") + (("beta",) if ln and with_beta else ())
+    names = ("x", "dy") if sm else ("x", "gamma", "dy") + (("beta",) if ln and with_beta else ())
     host_in = {k: inp[k].pin_memory() for k in names}
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
     hy = (torch.empty(host_in["x"].shape, dtype=torch.uint8) if f8
           else torch.empty_like(host_in["x"])).pin_memory()
     scale = torch.tensor([w.scale], dtype=torch.float32, device=dev)
     hdx = torch.empty_like(host_in["x"]).pin_memory()
-    stats = [torch.empty(w.rows, dtype=torch.float32).pin_memory() for _ in range(2 if ln else 1)]
+    stats = [torch.empty(w.rows, dtype=torch.float32).pin_memory()
+             for _ in range(0 if sm else 2 if ln else 1)]
     grads = [torch.empty(w.hidden, dtype=torch.float32).pin_memory()
-             for _ in range(2 if ln and with_beta else 1)]
+             for _ in range(0 if sm else 2 if ln and with_beta else 1)]
     ws_fn = L.layer_norm_bwd_workspace_size if ln else L.rms_norm_bwd_workspace_size
     ws = torch.empty(max(16, ws_fn(w.rows, w.hidden, host_in["x"].dtype)), dtype=torch.uint8,
                      device=dev)
@@ -504,8 +524,12 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
     def one():
         for k, v in host_in.items():
             dev_in[k].copy_(v, non_blocking=True)
-        x, g, dy = dev_in["x"], dev_in["gamma"], dev_in["dy"]
-        if ln:
+        x, g, dy = dev_in["x"], dev_in.get("gamma"), dev_in["dy"]
+        if sm:
+            y = L.softmax_fwd(x)
+            dx = L.softmax_bwd(dy, y)
+            outs = []
+        elif ln:
             y, mean, rstd = L.layer_norm_fwd(x, g, dev_in.get("beta"), w.eps)
             dx, dgam, dbet = L.layer_norm_bwd(dy, x, g, mean, rstd, with_dbeta=with_beta,
                                               workspace=ws)
@@ -596,7 +620,7 @@ def run_reference(args, rank, world, local):
               f"per step (numpy, single thread)")
     line = {
         "impl": "reference",
-        "metric": METRIC_LN if w.kind == "ln" else METRIC,
+        "metric": metric_for(w),
         "value": round(value, 5),
         "unit": "GB/s",
         "n_gpus": world,

@@ -17,6 +17,8 @@ The functions carry the names of the C entry points declared in
 * ``rms_norm_fwd_fp8(x, gamma, scale, eps, offset=0)`` -> ``(y8, rstd)``
   (``y8`` a torch.float8_e4m3fn tensor, ``scale`` a one-element fp32
   device tensor)
+* ``softmax_fwd(x)`` -> ``y``; ``softmax_bwd(dy, y)`` -> ``dx`` (last
+  dimension)
 * ``layer_norm_fwd(x, gamma, beta, eps)`` -> ``(y, mean, rstd)``
 * ``layer_norm_bwd(dy, x, gamma, mean, rstd)`` -> ``(dx, dgamma, dbeta)``
 """
@@ -54,6 +56,8 @@ EXPORTED = (
     "layer_norm_fwd",
     "layer_norm_bwd_workspace_size",
     "layer_norm_bwd",
+    "softmax_fwd",
+    "softmax_bwd",
 )
 
 
@@ -96,6 +100,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_wait_timeouts.restype = I
     lib.rms_norm_fwd_fp8.argtypes = [P, P, P, P, P, I64, I64, F, I, I, P]
     lib.rms_norm_fwd_fp8.restype = I
+    lib.softmax_fwd.argtypes = [P, P, I64, I64, I, P]
+    lib.softmax_fwd.restype = I
+    lib.softmax_bwd.argtypes = [P, P, P, I64, I64, I, P]
+    lib.softmax_bwd.restype = I
     lib.layer_norm_fwd.argtypes = [P, P, P, P, P, P, I64, I64, F, I, P]
     lib.layer_norm_fwd.restype = I
     lib.layer_norm_bwd_workspace_size.argtypes = [I64, I64, I]
@@ -357,3 +365,42 @@ def layer_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean:
     if st != RMSN_OK:
         raise RMSNormError("layer_norm_bwd", st)
     return dx, dgamma, (dbeta if with_dbeta else None)
+
+
+def softmax_fwd(x: torch.Tensor, y: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Softmax over the last dimension of ``x`` (fp32 arithmetic, one
+    rounding to x's dtype at the store)."""
+    lib = load_library()
+    _check_cuda("x", x)
+    rows, cols = _as_rows(x)
+    y = torch.empty_like(x) if y is None else y
+    _check_cuda("y", y)
+    if y.dtype != x.dtype or y.shape != x.shape:
+        raise RuntimeError("y must match x in dtype and shape")
+    with torch.cuda.device(x.device):
+        st = lib.softmax_fwd(_ptr(x), _ptr(y), rows, cols, DTYPE_CODES[x.dtype],
+                             _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("softmax_fwd", st)
+    return y
+
+
+def softmax_bwd(dy: torch.Tensor, y: torch.Tensor, dx: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Backward of softmax_fwd from its output: dx = y * (dy - sum(dy * y))
+    per row, the sum in fp32."""
+    lib = load_library()
+    _check_cuda("dy", dy)
+    _check_cuda("y", y)
+    if dy.dtype != y.dtype or dy.shape != y.shape:
+        raise RuntimeError("dy and y must share dtype and shape")
+    rows, cols = _as_rows(y)
+    dx = torch.empty_like(y) if dx is None else dx
+    _check_cuda("dx", dx)
+    with torch.cuda.device(y.device):
+        st = lib.softmax_bwd(_ptr(dy), _ptr(y), _ptr(dx), rows, cols, DTYPE_CODES[y.dtype],
+                             _stream_handle(y.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("softmax_bwd", st)
+    return dx

@@ -268,6 +268,47 @@ int layer_norm_bwd(const void* dy, const void* x, const void* gamma, const float
   return RMSN_OK;
 }
 
+int softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, int dtype, void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (rows < 0 || rows > RMSN_MAX_ROWS || cols < 1 || cols > RMSN_MAX_HIDDEN)
+    return RMSN_ERR_SHAPE;
+  t_last_launches = 0;
+  if (rows == 0) return RMSN_OK;
+  if (!x || !y) return RMSN_ERR_NULL;
+  SoftmaxArgs a{};
+  a.x = x;
+  a.y = y;
+  a.rows = rows;
+  a.cols = (int)cols;
+  a.vec_ok = ((cols * elem_bytes(dtype)) % 16 == 0) && aligned16(x) && aligned16(y);
+  cudaError_t e = launch_softmax_fwd(dtype, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = 1;
+  return RMSN_OK;
+}
+
+int softmax_bwd(const void* dy, const void* y, void* dx, int64_t rows, int64_t cols, int dtype,
+                void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (rows < 0 || rows > RMSN_MAX_ROWS || cols < 1 || cols > RMSN_MAX_HIDDEN)
+    return RMSN_ERR_SHAPE;
+  t_last_launches = 0;
+  if (rows == 0) return RMSN_OK;
+  if (!dy || !y || !dx) return RMSN_ERR_NULL;
+  SoftmaxArgs a{};
+  a.dy = dy;
+  a.y = y;
+  a.dx = dx;
+  a.rows = rows;
+  a.cols = (int)cols;
+  a.vec_ok = ((cols * elem_bytes(dtype)) % 16 == 0) && aligned16(dy) && aligned16(y) &&
+             aligned16(dx);
+  cudaError_t e = launch_softmax_bwd(dtype, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = 1;
+  return RMSN_OK;
+}
+
 const char* rms_norm_status_string(int status) {
   switch (status) {
     case RMSN_OK: return "ok";

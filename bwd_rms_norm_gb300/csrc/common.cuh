@@ -173,6 +173,26 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+  return v;
+}
+
+// Maximum of `v` over the whole CTA; same buffer and parity scheme as
+// block_sum below.
+__device__ __forceinline__ float block_max(float v, float* red, int parity) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = warp_max(v);
+  float* slot = red + 32 * parity;
+  if (lane == 0) slot[warp] = v;
+  __syncthreads();
+  float m = slot[0];
+  for (int w = 1; w < nwarps; ++w) m = fmaxf(m, slot[w]);
+  return m;
+}
+
 // Sum of `v` over the whole CTA.  `red` holds 2 x 32 floats; `parity`
 // alternates between calls so that one __syncthreads per call suffices: a
 // thread can only overwrite slot p after every thread has passed the barrier

@@ -129,6 +129,21 @@ bool try_launch_ln_bwd_tma(int dtype, const LnBwdArgs& a, cudaStream_t s, cudaEr
                            int* nparts);
 cudaError_t launch_ln_bwd(int dtype, const LnBwdArgs& a, cudaStream_t s, int* launches);
 
+// Inputs of one softmax call (forward: x -> y; backward: dy, y -> dx),
+// already validated (rows >= 1).
+struct SoftmaxArgs {
+  const void* x;
+  const void* y;   // forward: the output (written); backward: the input
+  const void* dy;
+  void* dx;
+  int64_t rows;
+  int cols;
+  bool vec_ok;
+};
+
+cudaError_t launch_softmax_fwd(int dtype, const SoftmaxArgs& a, cudaStream_t s);
+cudaError_t launch_softmax_bwd(int dtype, const SoftmaxArgs& a, cudaStream_t s);
+
 // Device properties, cached per device.
 int sm_count(int device);
 int max_blocks_per_sm(const void* func, int block, size_t smem);

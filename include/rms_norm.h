@@ -183,6 +183,30 @@ int layer_norm_bwd(const void* dy, const void* x, const void* gamma,
                    int dtype, void* workspace, size_t workspace_bytes,
                    void* stream);
 
+/*
+ * Softmax over the last dimension (candle PR #4059 "Add backward passes to
+ * the fused rms_norm, layer_norm and softmax_last_dim ops", description):
+ *
+ *   forward   y[r,j]  = round( exp(x[r,j] - m_r) / sum_k exp(x[r,k] - m_r) ),
+ *             m_r = max_k x[r,k]; exp, the sum and the division in fp32
+ *             (computed as exp(.) * (1 / sum)), one rounding at the store;
+ *   backward  dx[r,j] = round( y[r,j] * (dy[r,j] - sum_k dy[r,k] * y[r,k]) ),
+ *             from the forward's stored y, the sum in fp32.
+ *
+ * x, y, dy, dx: device, row-major [rows, cols], dtype (fp32/bf16/fp16),
+ * owned by the caller; 1 <= cols <= RMSN_MAX_HIDDEN.  rows == 0 is a no-op.
+ * A row of -inf (or one holding +inf) gives NaN, as the formula does.
+ * Vector kernels run when the pointers are 16-byte aligned and
+ * cols * sizeof(dtype) is a multiple of 16; otherwise scalar kernels.  One
+ * kernel launch each, no workspace.  Errors as the RMSNorm entry points
+ * (NULL pointers with rows > 0: RMSN_ERR_NULL; cols out of range:
+ * RMSN_ERR_SHAPE).
+ */
+int softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, int dtype,
+                void* stream);
+int softmax_bwd(const void* dy, const void* y, void* dx, int64_t rows,
+                int64_t cols, int dtype, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* rms_norm_status_string(int status);
 

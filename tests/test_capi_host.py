@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:rms|layer)_norm_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:rms_norm|layer_norm|softmax)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_entry_points():
@@ -167,3 +167,21 @@ def test_fp8_forward_validation(lib):
     for k in ("x", "g", "s", "y", "r"):
         assert f(**{k: NULL}) == 1, k
     assert f(rows=0, x=NULL, g=NULL, s=NULL, y=NULL, r=NULL) == 0
+
+
+def test_softmax_validation(lib):
+    """Host-side checks of softmax_fwd / softmax_bwd (every case rejected
+    before a launch, or rows == 0)."""
+    f = lambda **k: lib.softmax_fwd(k.get("x", FAKE), k.get("y", FAKE), k.get("rows", 4),
+                                    k.get("cols", 64), k.get("dtype", 1), None)
+    assert f(dtype=7) == 4
+    assert f(cols=0) == 2 and f(cols=65537) == 2 and f(rows=-2) == 2
+    assert f(x=NULL) == 1 and f(y=NULL) == 1
+    assert f(rows=0, x=NULL, y=NULL) == 0
+    b = lambda **k: lib.softmax_bwd(k.get("dy", FAKE), k.get("y", FAKE), k.get("dx", FAKE),
+                                    k.get("rows", 4), k.get("cols", 64), k.get("dtype", 1), None)
+    assert b(dtype=-1) == 4
+    assert b(cols=0) == 2
+    for k in ("dy", "y", "dx"):
+        assert b(**{k: NULL}) == 1, k
+    assert b(rows=0, dy=NULL, y=NULL, dx=NULL) == 0

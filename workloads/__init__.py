@@ -40,7 +40,7 @@ class Workload:
     gamma_dist: Dist
     dy_dist: Dist
     seed: int = 0
-    kind: str = "rms"                 # "rms" (RMSNorm) or "ln" (LayerNorm)
+    kind: str = "rms"                 # "rms", "ln" (LayerNorm), "softmax"
     beta_dist: Optional[Dist] = None  # LayerNorm bias; None: no bias
     out_fmt: Optional[str] = None     # "e4m3": FP8 forward output (RMSNorm)
     scale: float = 1.0                # per-tensor scale of the FP8 output
@@ -56,6 +56,8 @@ class Workload:
         """Bytes the forward must move: read x and gamma (and beta), write y
         and the fp32 row statistics (rstd; mean and rstd for LayerNorm)."""
         s, r, n = self.elem_bytes, self.rows, self.hidden
+        if self.kind == "softmax":
+            return 2 * r * n * s          # read x, write y
         if self.kind == "ln":
             nb = n * s if self.beta_dist is not None else 0
             return 2 * r * n * s + 8 * r + n * s + nb
@@ -68,6 +70,8 @@ class Workload:
         """Bytes the backward must move: read dy, x, gamma and the statistics,
         write dx and the fp32 weight (and bias) gradients."""
         s, r, n = self.elem_bytes, self.rows, self.hidden
+        if self.kind == "softmax":
+            return 3 * r * n * s          # read y and dy, write dx
         if self.kind == "ln":
             return 3 * r * n * s + 8 * r + n * s + 8 * n
         return 3 * r * n * s + 4 * r + n * s + 4 * n
@@ -177,3 +181,18 @@ def make_inputs(w: Workload, rows: Optional[int] = None) -> Dict[str, torch.Tens
 def as_float64(t: torch.Tensor):
     """The values of a CPU tensor as a float64 numpy array (exact widening)."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def softmax_workloads() -> Dict[str, Workload]:
+    """Softmax over the last dimension: logits x ~ N(0, 4) (std 2, the
+    spread of attention scores), dy ~ N(0, 1); the same shapes as the
+    RMSNorm workloads plus many short rows.  eps, offset, cast mode and
+    gamma are unused."""
+    def sm(name, rows, cols, dtype):
+        return Workload(name, rows, cols, dtype, 0.0, 0, "round_once", ("normal", 0.0, 4.0),
+                        ("zeros", 0.0, 0.0), _N01, kind="softmax")
+    ws = [sm("softmax_fp32_256x1024", 256, 1024, "f32"),
+          sm("softmax_bf16_4096x4096", 4096, 4096, "bf16"),
+          sm("softmax_bf16_16384x8192", 16384, 8192, "bf16"),
+          sm("softmax_f16_65536x1024", 65536, 1024, "f16")]
+    return {w.name: w for w in ws}
