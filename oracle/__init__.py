@@ -33,8 +33,14 @@ Parity status of each function (what pins it is in ``tests/test_oracle.py``):
   row whose exp overflows unshifted) and its autograd, finite differences,
   rows summing to 1, dx rows summing to 0, shift invariance, closed forms
   for one, two and constant elements, torch's CPU bf16 softmax.
+* ``group_norm.forward`` / ``backward`` (and the ``_exact`` forms) -- pinned
+  in ``tests/test_oracle_group_norm.py``: torch's CPU ``group_norm`` in
+  float64 and its autograd, finite differences (x, W, B), per-group sums of
+  dx and x_hat, the upstream-of-ones case of Liger-Kernel PR #1608 (dx = 0),
+  G = 1 against the LayerNorm oracle, G = C against torch's
+  ``instance_norm``, torch's CPU bf16 ``group_norm``.
 """
-from . import fp8, layer_norm, softmax  # noqa: F401
+from . import fp8, group_norm, layer_norm, softmax  # noqa: F401
 from .rounding import FORMATS, max_finite, round_to, ulp_distance  # noqa: F401
 from .rms_norm import (  # noqa: F401
     BF16,
