@@ -51,10 +51,11 @@ if ROOT not in sys.path:
 METRIC = "RMSNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
 METRIC_LN = "LayerNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
 METRIC_SM = "Softmax (last dim) fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
+METRIC_GN = "GroupNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per call"
 
 
 def metric_for(w) -> str:
-    return {"ln": METRIC_LN, "softmax": METRIC_SM}.get(w.kind, METRIC)
+    return {"ln": METRIC_LN, "softmax": METRIC_SM, "gn": METRIC_GN}.get(w.kind, METRIC)
 DEFAULT_WORKLOAD = "llama_bf16_4096x4096"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
@@ -187,13 +188,14 @@ _ORACLE_INPUTS = {}
 
 def workload_by_name(name: str):
     """RMSNorm workloads, the LayerNorm ones (names starting ``ln_``), the
-    FP8-output ones (names ending ``_fp8``) and the softmax ones (names
-    starting ``softmax_``)."""
+    FP8-output ones (names ending ``_fp8``), the softmax ones (names
+    starting ``softmax_``) and the GroupNorm ones (names starting ``gn_``)."""
     import workloads as W
     table = dict(W.all_workloads())
     table.update(W.layer_norm_workloads())
     table.update(W.fp8_workloads())
     table.update(W.softmax_workloads())
+    table.update(W.group_norm_workloads())
     if name not in table:
         raise SystemExit(f"unknown workload {name!r}; known: {', '.join(sorted(table))}")
     return table[name]
@@ -204,6 +206,7 @@ def time_oracle(w, rows: int):
     (inputs drawn once per row count, outside the timing)."""
     import workloads as W
     from oracle import fp8 as of8
+    from oracle import group_norm as ogn
     from oracle import layer_norm as oln
     from oracle import rms_norm as orm
     from oracle import softmax as osm
@@ -218,6 +221,9 @@ def time_oracle(w, rows: int):
     if ws.kind == "softmax":
         y = osm.forward(xd, ws.dtype)
         osm.backward(dyd, y, ws.dtype)
+    elif ws.kind == "gn":
+        _, mean, rstd = ogn.forward(xd, gd, bd, ws.groups, ws.eps, ws.dtype)
+        ogn.backward(dyd, xd, gd, mean, rstd, ws.groups, ws.dtype)
     elif ws.kind == "ln":
         _, mean, rstd = oln.forward(xd, gd, bd, ws.eps, ws.dtype)
         oln.backward(dyd, xd, gd, mean, rstd, ws.dtype)
@@ -252,15 +258,17 @@ def run_ours(args, rank, world, local):
         w = w.with_(rows=args.rows)
     ln = w.kind == "ln"
     sm = w.kind == "softmax"
+    gn = w.kind == "gn"
     f8 = w.out_fmt == "e4m3"
     inp = W.make_inputs(w)
+    nstat = w.rows * (w.groups if gn else 1)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or (126 << 20))
 
     # Several copies of the batch, cycled, so that every step finds its
     # inputs evicted from L2 by the other copies' traffic (at least six L2
     # sizes of data in the cycle).
-    set_bytes = 4 * w.rows * w.hidden * w.elem_bytes + (8 if ln else 4) * w.rows
+    set_bytes = 4 * w.rows * w.hidden * w.elem_bytes + 8 * nstat
     nsets = max(2, min(8, math.ceil(6 * l2 / set_bytes)))
     sets = []
     for _ in range(nsets):
@@ -268,21 +276,29 @@ def run_ours(args, rank, world, local):
         y = (torch.empty(x.shape, dtype=L.FP8_DTYPE, device=dev) if f8 else torch.empty_like(x))
         sets.append({"x": x, "dy": inp["dy"].to(dev), "y": y,
                      "dx": torch.empty_like(x),
-                     "rstd": torch.empty(w.rows, dtype=torch.float32, device=dev),
-                     "mean": torch.empty(w.rows, dtype=torch.float32, device=dev)})
+                     "rstd": torch.empty(nstat, dtype=torch.float32, device=dev),
+                     "mean": torch.empty(nstat, dtype=torch.float32, device=dev)})
     g = inp["gamma"].to(dev)
     beta = inp["beta"].to(dev) if "beta" in inp else None
     scale = torch.tensor([w.scale], dtype=torch.float32, device=dev)
-    dw = torch.empty(w.hidden, dtype=torch.float32, device=dev)
-    db = torch.empty(w.hidden, dtype=torch.float32, device=dev)
-    ws_fn = L.layer_norm_bwd_workspace_size if ln else L.rms_norm_bwd_workspace_size
-    ws = torch.empty(max(16, ws_fn(w.rows, w.hidden, g.dtype)), dtype=torch.uint8, device=dev)
+    dw = torch.empty(w.param_len, dtype=torch.float32, device=dev)
+    db = torch.empty(w.param_len, dtype=torch.float32, device=dev)
+    if gn:
+        ws_bytes = L.group_norm_bwd_workspace_size(w.rows, w.channels, w.spatial, w.groups,
+                                                   g.dtype)
+    else:
+        ws_fn = L.layer_norm_bwd_workspace_size if ln else L.rms_norm_bwd_workspace_size
+        ws_bytes = 0 if sm else ws_fn(w.rows, w.hidden, g.dtype)
+    ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
     half = nsets // 2
 
     def fwd(k):
         S = sets[k]
         if sm:
             L.softmax_fwd(S["x"], y=S["y"])
+        elif gn:
+            L.group_norm_fwd(S["x"], g, beta, w.groups, w.eps, y=S["y"], mean=S["mean"],
+                             rstd=S["rstd"])
         elif ln:
             L.layer_norm_fwd(S["x"], g, beta, w.eps, y=S["y"], mean=S["mean"], rstd=S["rstd"])
         elif f8:
@@ -294,6 +310,9 @@ def run_ours(args, rank, world, local):
         S = sets[k]
         if sm:
             L.softmax_bwd(S["dy"], S["y"], dx=S["dx"])
+        elif gn:
+            L.group_norm_bwd(S["dy"], S["x"], g, S["mean"], S["rstd"], w.groups, dx=S["dx"],
+                             dgamma=dw, dbeta=db, workspace=ws)
         elif ln:
             L.layer_norm_bwd(S["dy"], S["x"], g, S["mean"], S["rstd"], dx=S["dx"], dgamma=dw,
                              dbeta=db, workspace=ws)
@@ -406,7 +425,7 @@ def run_ours(args, rank, world, local):
                "sample": f"{args.workload}: {passes} float64 forward+backward passes over all "
                          f"{w.rows} rows ({secs:.1f} s, numpy, single thread)"}
 
-    op = "layer_norm" if ln else "softmax" if sm else "rms_norm"
+    op = "layer_norm" if ln else "softmax" if sm else "group_norm" if gn else "rms_norm"
     fwd_name = f"{op}_fwd" + ("_fp8" if f8 else "")
     line = {
         "metric": metric_for(w),
@@ -426,8 +445,10 @@ def run_ours(args, rank, world, local):
             "rows": w.rows, "hidden": w.hidden,
             **({"arith": "fp32 exp/sum/dot, one rounding at each store"} if sm else
                {"eps": w.eps, "stats": "fp32", "rstd": "fp32", "dw": "fp32"}),
-            **({"bias": beta is not None, "mean": "fp32", "dbeta": "fp32"} if ln else {}),
-            **({"offset": w.offset, "cast_mode": w.cast_mode} if not (ln or sm) else {}),
+            **({"bias": beta is not None, "mean": "fp32", "dbeta": "fp32"} if ln or gn else {}),
+            **({"samples": w.rows, "channels": w.channels, "spatial": w.spatial,
+                "groups": w.groups} if gn else {}),
+            **({"offset": w.offset, "cast_mode": w.cast_mode} if not (ln or sm or gn) else {}),
             **({"y": "fp8 e4m3 (saturating)", "scale": w.scale} if f8 else {}),
             "global_batch_rows": w.rows * world,
             "parallelism": f"replica x{world} (one batch per rank)",
@@ -505,21 +526,28 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
     import torch
     ln = w.kind == "ln"
     sm = w.kind == "softmax"
+    gn = w.kind == "gn"
     f8 = w.out_fmt == "e4m3"
-    names = ("x", "dy") if sm else ("x", "gamma", "dy") + (("beta",) if ln and with_beta else ())
+    names = ("x", "dy") if sm else ("x", "gamma", "dy") + (("beta",) if (ln or gn) and with_beta
+                                                           else ())
     host_in = {k: inp[k].pin_memory() for k in names}
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
     hy = (torch.empty(host_in["x"].shape, dtype=torch.uint8) if f8
           else torch.empty_like(host_in["x"])).pin_memory()
     scale = torch.tensor([w.scale], dtype=torch.float32, device=dev)
     hdx = torch.empty_like(host_in["x"]).pin_memory()
-    stats = [torch.empty(w.rows, dtype=torch.float32).pin_memory()
-             for _ in range(0 if sm else 2 if ln else 1)]
-    grads = [torch.empty(w.hidden, dtype=torch.float32).pin_memory()
-             for _ in range(0 if sm else 2 if ln and with_beta else 1)]
-    ws_fn = L.layer_norm_bwd_workspace_size if ln else L.rms_norm_bwd_workspace_size
-    ws = torch.empty(max(16, ws_fn(w.rows, w.hidden, host_in["x"].dtype)), dtype=torch.uint8,
-                     device=dev)
+    nstat = w.rows * (w.groups if gn else 1)
+    stats = [torch.empty(nstat, dtype=torch.float32).pin_memory()
+             for _ in range(0 if sm else 2 if ln or gn else 1)]
+    grads = [torch.empty(w.param_len, dtype=torch.float32).pin_memory()
+             for _ in range(0 if sm else 2 if (ln or gn) and with_beta else 1)]
+    if gn:
+        ws_bytes = L.group_norm_bwd_workspace_size(w.rows, w.channels, w.spatial, w.groups,
+                                                   host_in["x"].dtype)
+    else:
+        ws_fn = L.layer_norm_bwd_workspace_size if ln else L.rms_norm_bwd_workspace_size
+        ws_bytes = 0 if sm else ws_fn(w.rows, w.hidden, host_in["x"].dtype)
+    ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
 
     def one():
         for k, v in host_in.items():
@@ -529,6 +557,11 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
             y = L.softmax_fwd(x)
             dx = L.softmax_bwd(dy, y)
             outs = []
+        elif gn:
+            y, mean, rstd = L.group_norm_fwd(x, g, dev_in.get("beta"), w.groups, w.eps)
+            dx, dgam, dbet = L.group_norm_bwd(dy, x, g, mean, rstd, w.groups,
+                                              with_dbeta=with_beta, workspace=ws)
+            outs = [mean.view(-1), rstd.view(-1), dgam] + ([dbet] if with_beta else [])
         elif ln:
             y, mean, rstd = L.layer_norm_fwd(x, g, dev_in.get("beta"), w.eps)
             dx, dgam, dbet = L.layer_norm_bwd(dy, x, g, mean, rstd, with_dbeta=with_beta,
@@ -603,10 +636,11 @@ def run_reference(args, rank, world, local):
         return
     w = workload_by_name(args.workload)
     # size the sample so that warmup + steps take about two minutes
-    probe, _ = time_oracle(w, 64)
-    per_row = probe / 64
+    nprobe = max(1, min(64, (1 << 22) // w.hidden))
+    probe, _ = time_oracle(w, nprobe)
+    per_row = probe / nprobe
     budget = 120.0 / max(1, args.steps + args.warmup)
-    rows = int(max(16, min(w.rows, budget / per_row)))
+    rows = int(max(min(16, w.rows), min(w.rows, budget / per_row)))
     for _ in range(args.warmup):
         time_oracle(w, rows)
     times = []

@@ -19,6 +19,9 @@ The functions carry the names of the C entry points declared in
   device tensor)
 * ``softmax_fwd(x)`` -> ``y``; ``softmax_bwd(dy, y)`` -> ``dx`` (last
   dimension)
+* ``group_norm_fwd(x, gamma, beta, groups, eps)`` -> ``(y, mean, rstd)``;
+  ``group_norm_bwd(dy, x, gamma, mean, rstd, groups)`` ->
+  ``(dx, dgamma, dbeta)`` (x of shape [n, channels, *spatial])
 * ``layer_norm_fwd(x, gamma, beta, eps)`` -> ``(y, mean, rstd)``
 * ``layer_norm_bwd(dy, x, gamma, mean, rstd)`` -> ``(dx, dgamma, dbeta)``
 """
@@ -58,6 +61,9 @@ EXPORTED = (
     "layer_norm_bwd",
     "softmax_fwd",
     "softmax_bwd",
+    "group_norm_fwd",
+    "group_norm_bwd_workspace_size",
+    "group_norm_bwd",
 )
 
 
@@ -100,6 +106,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_wait_timeouts.restype = I
     lib.rms_norm_fwd_fp8.argtypes = [P, P, P, P, P, I64, I64, F, I, I, P]
     lib.rms_norm_fwd_fp8.restype = I
+    lib.group_norm_fwd.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, F, I, P]
+    lib.group_norm_fwd.restype = I
+    lib.group_norm_bwd_workspace_size.argtypes = [I64, I64, I64, I64, I]
+    lib.group_norm_bwd_workspace_size.restype = SZ
+    lib.group_norm_bwd.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, I64, I, P, SZ, P]
+    lib.group_norm_bwd.restype = I
     lib.softmax_fwd.argtypes = [P, P, I64, I64, I, P]
     lib.softmax_fwd.restype = I
     lib.softmax_bwd.argtypes = [P, P, P, I64, I64, I, P]
@@ -404,3 +416,82 @@ def softmax_bwd(dy: torch.Tensor, y: torch.Tensor, dx: Optional[torch.Tensor] = 
     if st != RMSN_OK:
         raise RMSNormError("softmax_bwd", st)
     return dx
+
+
+def _gn_shape(x: torch.Tensor, groups: int):
+    if x.dim() < 2:
+        raise RuntimeError("x must be [n, channels, *spatial]")
+    n, c = x.shape[0], x.shape[1]
+    spatial = 1
+    for d in x.shape[2:]:
+        spatial *= d
+    if c % groups:
+        raise RuntimeError("channels must be a multiple of groups")
+    return n, c, spatial
+
+
+def group_norm_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Tensor],
+                   groups: int, eps: float, y: Optional[torch.Tensor] = None,
+                   mean: Optional[torch.Tensor] = None, rstd: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """GroupNorm forward over x [n, channels, *spatial]; returns ``(y, mean,
+    rstd)`` with mean and rstd fp32 [n, groups] (``beta`` may be None)."""
+    lib = load_library()
+    _check_cuda("x", x)
+    _check_cuda("gamma", gamma)
+    n, c, sp = _gn_shape(x, groups)
+    if gamma.dtype != x.dtype or gamma.numel() != c:
+        raise RuntimeError("gamma must have the dtype of x and one value per channel")
+    if beta is not None:
+        _check_cuda("beta", beta)
+        if beta.dtype != x.dtype or beta.numel() != c:
+            raise RuntimeError("beta must have the dtype of x and one value per channel")
+    y = torch.empty_like(x) if y is None else y
+    mean = torch.empty(n, groups, dtype=torch.float32, device=x.device) if mean is None else mean
+    rstd = torch.empty(n, groups, dtype=torch.float32, device=x.device) if rstd is None else rstd
+    with torch.cuda.device(x.device):
+        st = lib.group_norm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
+                                n, c, sp, int(groups), float(eps), DTYPE_CODES[x.dtype],
+                                _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("group_norm_fwd", st)
+    return y, mean, rstd
+
+
+def group_norm_bwd_workspace_size(n: int, channels: int, spatial: int, groups: int,
+                                  dtype) -> int:
+    code = DTYPE_CODES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load_library().group_norm_bwd_workspace_size(int(n), int(channels), int(spatial),
+                                                            int(groups), code))
+
+
+def group_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean: torch.Tensor,
+                   rstd: torch.Tensor, groups: int, dx: Optional[torch.Tensor] = None,
+                   dgamma: Optional[torch.Tensor] = None, dbeta: Optional[torch.Tensor] = None,
+                   with_dbeta: bool = True, workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """GroupNorm backward; returns ``(dx, dgamma, dbeta)`` (fp32 weight
+    gradients; dbeta None when ``with_dbeta`` is False)."""
+    lib = load_library()
+    for name, t in (("dy", dy), ("x", x), ("gamma", gamma), ("mean", mean), ("rstd", rstd)):
+        _check_cuda(name, t)
+    if dy.dtype != x.dtype or gamma.dtype != x.dtype or dy.shape != x.shape:
+        raise RuntimeError("dy, x and gamma must share one dtype; dy shaped like x")
+    n, c, sp = _gn_shape(x, groups)
+    code = DTYPE_CODES[x.dtype]
+    dx = torch.empty_like(x) if dx is None else dx
+    dgamma = torch.empty(c, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
+    if with_dbeta and dbeta is None:
+        dbeta = torch.empty(c, dtype=torch.float32, device=x.device)
+    need = int(lib.group_norm_bwd_workspace_size(n, c, sp, int(groups), code))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(x.device):
+        st = lib.group_norm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
+                                _ptr(dgamma), _ptr(dbeta) if with_dbeta else None, n, c, sp,
+                                int(groups), code, workspace.data_ptr(), ws_bytes,
+                                _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("group_norm_bwd", st)
+    return dx, dgamma, (dbeta if with_dbeta else None)

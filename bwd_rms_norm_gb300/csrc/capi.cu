@@ -1,6 +1,7 @@
 // C ABI of the fused RMSNorm library: argument validation and dispatch.
 // Every check runs on the host before anything is enqueued.
 #include <math.h>
+#include <stdint.h>
 
 #include <atomic>
 #include <mutex>
@@ -306,6 +307,94 @@ int softmax_bwd(const void* dy, const void* y, void* dx, int64_t rows, int64_t c
   cudaError_t e = launch_softmax_bwd(dtype, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   t_last_launches = 1;
+  return RMSN_OK;
+}
+
+namespace {
+// Shape check shared by the GroupNorm entry points.
+bool gn_shape_ok(int64_t n, int64_t channels, int64_t spatial, int64_t groups) {
+  if (n < 0 || channels < 1 || spatial < 1 || groups < 1) return false;
+  if (channels > (1 << 24) || spatial > (1 << 30) || channels % groups != 0) return false;
+  if ((channels / groups) * spatial > (1 << 30)) return false;
+  if (n * groups > RMSN_MAX_ROWS) return false;
+  return n <= (INT64_MAX / channels) / spatial;
+}
+}  // namespace
+
+int group_norm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
+                   float* rstd, int64_t n, int64_t channels, int64_t spatial, int64_t groups,
+                   float eps, int dtype, void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (!gn_shape_ok(n, channels, spatial, groups)) return RMSN_ERR_SHAPE;
+  if (!(eps >= 0.f) || isinf(eps)) return RMSN_ERR_EPS;
+  t_last_launches = 0;
+  if (n == 0) return RMSN_OK;
+  if (!x || !gamma || !y || !mean || !rstd) return RMSN_ERR_NULL;
+  GnArgs a{};
+  a.x = x;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.y = y;
+  a.mean = mean;
+  a.rstd = rstd;
+  a.n = n;
+  a.channels = (int)channels;
+  a.spatial = (int)spatial;
+  a.groups = (int)groups;
+  a.eps = eps;
+  a.vec_ok = ((spatial * elem_bytes(dtype)) % 16 == 0) && aligned16(x) && aligned16(y);
+  cudaError_t e = launch_gn_fwd(dtype, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = 1;
+  return RMSN_OK;
+}
+
+size_t group_norm_bwd_workspace_size(int64_t n, int64_t channels, int64_t spatial,
+                                     int64_t groups, int dtype) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return 0;
+  if (!gn_shape_ok(n, channels, spatial, groups) || n == 0) return 0;
+  // partial rows: up to 16 (the largest cluster) per sample, dW and dB
+  return (size_t)n * 16u * 2u * (size_t)channels * sizeof(float);
+}
+
+int group_norm_bwd(const void* dy, const void* x, const void* gamma, const float* mean,
+                   const float* rstd, void* dx, float* dgamma, float* dbeta, int64_t n,
+                   int64_t channels, int64_t spatial, int64_t groups, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (!gn_shape_ok(n, channels, spatial, groups)) return RMSN_ERR_SHAPE;
+  t_last_launches = 0;
+  if (!dgamma) return RMSN_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n == 0) {
+    cudaError_t e = cudaMemsetAsync(dgamma, 0, (size_t)channels * sizeof(float), st);
+    if (e == cudaSuccess && dbeta) e = cudaMemsetAsync(dbeta, 0, (size_t)channels * sizeof(float), st);
+    return e == cudaSuccess ? RMSN_OK : cuda_fail(e);
+  }
+  if (!dy || !x || !gamma || !mean || !rstd || !dx || !workspace) return RMSN_ERR_NULL;
+  if (!aligned16(workspace)) return RMSN_ERR_ALIGN;
+  if (workspace_bytes < group_norm_bwd_workspace_size(n, channels, spatial, groups, dtype))
+    return RMSN_ERR_WORKSPACE;
+  GnArgs a{};
+  a.dy = dy;
+  a.x = x;
+  a.gamma = gamma;
+  a.mean = const_cast<float*>(mean);
+  a.rstd = const_cast<float*>(rstd);
+  a.dx = dx;
+  a.dgamma = dgamma;
+  a.dbeta = dbeta;
+  a.partial = static_cast<float*>(workspace);
+  a.n = n;
+  a.channels = (int)channels;
+  a.spatial = (int)spatial;
+  a.groups = (int)groups;
+  a.vec_ok = ((spatial * elem_bytes(dtype)) % 16 == 0) && aligned16(dy) && aligned16(x) &&
+             aligned16(dx);
+  int launches = 0;
+  cudaError_t e = launch_gn_bwd(dtype, a, st, &launches);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = launches;
   return RMSN_OK;
 }
 

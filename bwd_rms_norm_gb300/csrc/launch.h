@@ -144,6 +144,29 @@ struct SoftmaxArgs {
 cudaError_t launch_softmax_fwd(int dtype, const SoftmaxArgs& a, cudaStream_t s);
 cudaError_t launch_softmax_bwd(int dtype, const SoftmaxArgs& a, cudaStream_t s);
 
+// Inputs of one GroupNorm call over x [n, channels, spatial] with `groups`
+// groups of consecutive channels, already validated (n >= 1).
+struct GnArgs {
+  const void* x;
+  const void* gamma;
+  const void* beta;   // forward, may be NULL
+  void* y;
+  float* mean;        // [n, groups] fp32 (forward: written; backward: read)
+  float* rstd;
+  const void* dy;
+  void* dx;
+  float* dgamma;
+  float* dbeta;       // may be NULL (not computed)
+  float* partial;     // backward workspace, [n * 16, 2 * channels] fp32 at most
+  int64_t n;
+  int channels, spatial, groups;
+  float eps;
+  bool vec_ok;        // 16-byte aligned tensors and spatial * sizeof(T) % 16 == 0
+};
+
+cudaError_t launch_gn_fwd(int dtype, const GnArgs& a, cudaStream_t s);
+cudaError_t launch_gn_bwd(int dtype, const GnArgs& a, cudaStream_t s, int* launches);
+
 // Device properties, cached per device.
 int sm_count(int device);
 int max_blocks_per_sm(const void* func, int block, size_t smem);

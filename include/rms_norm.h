@@ -207,6 +207,50 @@ int softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, int dtype,
 int softmax_bwd(const void* dy, const void* y, void* dx, int64_t rows,
                 int64_t cols, int dtype, void* stream);
 
+/*
+ * GroupNorm (Liger-Kernel PR #1608 "fix(group_norm): keep the backward
+ * statistics and reductions in fp32": Mean and RSTD stored in fp32, the
+ * backward's reductions in fp32).  x is [n, channels, spatial] row-major
+ * (spatial = the flattened positions, e.g. H * W); the channels form
+ * `groups` groups of channels / groups consecutive channels.  For each
+ * sample i and group g, over the group's channels and positions:
+ *
+ *   mean[i,g] = average of x;  var = average of (x - mean)^2 (biased);
+ *   rstd[i,g] = 1 / sqrt(var + eps)                      (fp32, stored fp32)
+ *   y[i,c,s]  = round( (x[i,c,s] - mean) * rstd * gamma[c] + beta[c] )
+ *
+ * backward, with g = dy * gamma[c] and x_hat = (x - mean) * rstd:
+ *
+ *   dx = round( rstd * (g - avg_group(g) - x_hat * avg_group(g * x_hat)) )
+ *   dgamma[c] = sum over samples and positions of dy * x_hat      (fp32)
+ *   dbeta[c]  = sum over samples and positions of dy              (fp32)
+ *
+ * x, y, dy, dx: device, dtype (fp32/bf16/fp16); gamma, beta: device,
+ * [channels] of the same dtype (beta may be NULL: no bias); mean, rstd:
+ * device, [n, groups] fp32; dgamma, dbeta: device [channels] fp32,
+ * overwritten (dbeta may be NULL: not computed).  Shapes: n >= 0,
+ * channels % groups == 0, channels <= 2^24, (channels / groups) * spatial
+ * <= 2^30, else RMSN_ERR_SHAPE.  n == 0: nothing to compute (the backward
+ * zero-fills dgamma and dbeta).  The workspace holds fp32 partial rows of
+ * the weight gradients (group_norm_bwd_workspace_size bytes, 16-byte
+ * aligned); the result is reduced from them in a fixed order, so repeated
+ * calls give bit-identical dgamma and dbeta.  Vector kernels (a thread-block
+ * cluster of up to 16 CTAs per group) run when spatial * sizeof(dtype) is a
+ * multiple of 16 and x, y (dy, dx) are 16-byte aligned; otherwise scalar
+ * kernels.  Errors as the RMSNorm entry points.
+ */
+int group_norm_fwd(const void* x, const void* gamma, const void* beta, void* y,
+                   float* mean, float* rstd, int64_t n, int64_t channels,
+                   int64_t spatial, int64_t groups, float eps, int dtype,
+                   void* stream);
+size_t group_norm_bwd_workspace_size(int64_t n, int64_t channels, int64_t spatial,
+                                     int64_t groups, int dtype);
+int group_norm_bwd(const void* dy, const void* x, const void* gamma,
+                   const float* mean, const float* rstd, void* dx,
+                   float* dgamma, float* dbeta, int64_t n, int64_t channels,
+                   int64_t spatial, int64_t groups, int dtype, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* rms_norm_status_string(int status);
 

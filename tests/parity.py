@@ -14,7 +14,11 @@ within a relative 1e-3.  The readings of these numbers used here:
 * for half outputs the same floor applies -- an element passes with at most
   one ulp OR with |got - ref| <= 1e-5 * s; at most ceil(0.1% of n) of the n
   compared elements may differ from the reference at all (99.9% identical as
-  a rate, which a sample under 1000 elements cannot show otherwise);
+  a rate, which a sample under 1000 elements cannot show otherwise).  The
+  rate counts only elements with |ref| > 2**-10 * s: below that, the value
+  left after cancellation is within a few hundred fp32 rounding errors of
+  the terms, and no fp32 computation decides its half-precision rounding
+  (GroupNorm's dx for an upstream of ones is such a case throughout);
 * round twice rounds x_hat to the storage type, a decision the kernel takes
   on its fp32 x_hat.  Where the exact x_hat lies so close to a rounding
   midpoint that an fp32 x_hat (relative error well under 4e-6) may fall on
@@ -34,6 +38,7 @@ REL_DW = 1e-3
 MIN_BIT_IDENTICAL = 0.999
 FLOOR_REL = 1e-5
 MIDPOINT_WINDOW = 4e-6
+RESOLVABLE_REL = 2.0 ** -10
 
 
 def _row_rms(ref: np.ndarray) -> np.ndarray:
@@ -64,7 +69,8 @@ def check_rows(got: np.ndarray, ref: np.ndarray, fmt: str, alt=None, what="y", t
         if alt is not None:
             for mask, vals in alt:
                 ok |= mask & (got == vals)
-        same = float(np.mean(ulps == 0))
+        resolvable = np.abs(ref) > RESOLVABLE_REL * scale
+        same = float(np.mean(ulps[resolvable] == 0)) if np.any(resolvable) else 1.0
         worst_ulp = int(ulps.max()) if ulps.size else 0
     bad = np.argwhere(~ok)
     if bad.size:
@@ -75,7 +81,7 @@ def check_rows(got: np.ndarray, ref: np.ndarray, fmt: str, alt=None, what="y", t
     if fmt != "f32":
         # the fraction is a rate: below 1000 compared elements one element
         # that rounds the other way is already 0.1%, so allow ceil(0.1% n)
-        n = got.size
+        n = int(np.count_nonzero(resolvable))
         allowed = int(np.ceil((1.0 - MIN_BIT_IDENTICAL) * n - 1e-9))
         differ = int(round((1.0 - same) * n))
         assert differ <= allowed, f"{what}: only {same:.5f} bit-identical ({differ} of {n})"

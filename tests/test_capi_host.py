@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:rms_norm|layer_norm|softmax)_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:rms_norm|layer_norm|softmax|group_norm)_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_entry_points():
@@ -185,3 +185,36 @@ def test_softmax_validation(lib):
     for k in ("dy", "y", "dx"):
         assert b(**{k: NULL}) == 1, k
     assert b(rows=0, dy=NULL, y=NULL, dx=NULL) == 0
+
+
+def test_group_norm_validation(lib):
+    """Host-side checks of the GroupNorm entry points (every case rejected
+    before a launch, or n == 0)."""
+    def f(**k):
+        return lib.group_norm_fwd(k.get("x", FAKE), k.get("g", FAKE), k.get("b", NULL),
+                                  k.get("y", FAKE), k.get("m", FAKE), k.get("r", FAKE),
+                                  k.get("n", 2), k.get("c", 8), k.get("s", 64), k.get("G", 4),
+                                  k.get("eps", 1e-5), k.get("dtype", 1), None)
+    assert f(dtype=3) == 4
+    assert f(c=6, G=4) == 2          # channels not a multiple of groups
+    assert f(G=0) == 2 and f(s=0) == 2 and f(c=0) == 2 and f(n=-1) == 2
+    assert f(c=2, G=2, s=(1 << 30) + 8) == 2
+    assert f(eps=-1.0) == 3
+    for k in ("x", "g", "y", "m", "r"):
+        assert f(**{k: NULL}) == 1, k
+    assert f(n=0, x=NULL, g=NULL, y=NULL, m=NULL, r=NULL) == 0
+    assert lib.group_norm_bwd_workspace_size(2, 8, 64, 4, 1) == 2 * 16 * 2 * 8 * 4
+    assert lib.group_norm_bwd_workspace_size(2, 8, 64, 3, 1) == 0
+
+    def b(**k):
+        ws_bytes = k.get("ws_bytes", lib.group_norm_bwd_workspace_size(2, 8, 64, 4, 1))
+        return lib.group_norm_bwd(k.get("dy", FAKE), k.get("x", FAKE), k.get("g", FAKE),
+                                  k.get("m", FAKE), k.get("r", FAKE), k.get("dx", FAKE),
+                                  k.get("dg", FAKE), k.get("db", NULL), 2, 8, 64, 4,
+                                  k.get("dtype", 1), k.get("ws", FAKE), ws_bytes, None)
+    assert b(dtype=9) == 4
+    assert b(dg=NULL) == 1
+    for k in ("dy", "x", "g", "m", "r", "dx", "ws"):
+        assert b(**{k: NULL}) == 1, k
+    assert b(ws=ctypes.c_void_p(0x1004)) == 5
+    assert b(ws_bytes=64) == 6

@@ -44,6 +44,17 @@ class Workload:
     beta_dist: Optional[Dist] = None  # LayerNorm bias; None: no bias
     out_fmt: Optional[str] = None     # "e4m3": FP8 forward output (RMSNorm)
     scale: float = 1.0                # per-tensor scale of the FP8 output
+    channels: int = 0                 # GroupNorm: rows = samples, hidden = channels * spatial
+    groups: int = 0
+
+    @property
+    def spatial(self) -> int:
+        return self.hidden // self.channels if self.channels else 0
+
+    @property
+    def param_len(self) -> int:
+        """Length of gamma / beta: one per channel for GroupNorm."""
+        return self.channels if self.kind == "gn" else self.hidden
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -58,6 +69,9 @@ class Workload:
         s, r, n = self.elem_bytes, self.rows, self.hidden
         if self.kind == "softmax":
             return 2 * r * n * s          # read x, write y
+        if self.kind == "gn":
+            nb = self.channels * s if self.beta_dist is not None else 0
+            return 2 * r * n * s + 8 * r * self.groups + self.channels * s + nb
         if self.kind == "ln":
             nb = n * s if self.beta_dist is not None else 0
             return 2 * r * n * s + 8 * r + n * s + nb
@@ -72,6 +86,8 @@ class Workload:
         s, r, n = self.elem_bytes, self.rows, self.hidden
         if self.kind == "softmax":
             return 3 * r * n * s          # read y and dy, write dx
+        if self.kind == "gn":
+            return 3 * r * n * s + 8 * r * self.groups + self.channels * s + 8 * self.channels
         if self.kind == "ln":
             return 3 * r * n * s + 8 * r + n * s + 8 * n
         return 3 * r * n * s + 4 * r + n * s + 4 * n
@@ -159,6 +175,8 @@ def _draw(shape, dist: Dist, seed: int) -> torch.Tensor:
         return t * (b - a) + a
     if kind == "zeros":
         return torch.zeros(shape, dtype=torch.float32)
+    if kind == "const":
+        return torch.full(shape, float(a), dtype=torch.float32)
     raise ValueError(f"unknown distribution {kind!r}")
 
 
@@ -170,11 +188,14 @@ def make_inputs(w: Workload, rows: Optional[int] = None) -> Dict[str, torch.Tens
     r = w.rows if rows is None else rows
     dt = DTYPES[w.dtype]
     x = _draw((r, w.hidden), w.x_dist, w.seed + 0).to(dt)
-    gamma = _draw((w.hidden,), w.gamma_dist, w.seed + 1).to(dt)
+    gamma = _draw((w.param_len,), w.gamma_dist, w.seed + 1).to(dt)
     dy = _draw((r, w.hidden), w.dy_dist, w.seed + 2).to(dt)
     out = {"x": x, "gamma": gamma, "dy": dy}
     if w.beta_dist is not None:
-        out["beta"] = _draw((w.hidden,), w.beta_dist, w.seed + 3).to(dt)
+        out["beta"] = _draw((w.param_len,), w.beta_dist, w.seed + 3).to(dt)
+    if w.kind == "gn":
+        for k in ("x", "dy"):
+            out[k] = out[k].view(r, w.channels, w.spatial)
     return out
 
 
@@ -195,4 +216,30 @@ def softmax_workloads() -> Dict[str, Workload]:
           sm("softmax_bf16_4096x4096", 4096, 4096, "bf16"),
           sm("softmax_bf16_16384x8192", 16384, 8192, "bf16"),
           sm("softmax_f16_65536x1024", 65536, 1024, "f16")]
+    return {w.name: w for w in ws}
+
+
+def group_norm(name, n, c, spatial, groups, dtype, x_dist=_N01, dy_dist=_N01,
+               gamma_dist=_U0911, beta_dist=("normal", 0.0, 0.01), seed=0) -> Workload:
+    """GroupNorm over x [n, c, spatial]: rows = n, hidden = c * spatial."""
+    return Workload(name, n, c * spatial, dtype, 1e-5, 0, "round_once", x_dist, gamma_dist,
+                    dy_dist, seed=seed, kind="gn", beta_dist=beta_dist, channels=c,
+                    groups=groups)
+
+
+def group_norm_workloads() -> Dict[str, Workload]:
+    """The shapes Liger-Kernel PR #1608 times on B200 (x of (n, C, H, W) with
+    H * W flattened, or (n, C, L)), in bf16, plus its fp16 case with an
+    upstream gradient of ones and unit weights (where a channel sum in fp16
+    overflows) and an input offset of 16."""
+    ws = [group_norm("gn_bf16_16x32x256x256_g8", 16, 32, 256 * 256, 8, "bf16"),
+          group_norm("gn_fp32_16x32x256x256_g8", 16, 32, 256 * 256, 8, "f32"),
+          group_norm("gn_bf16_1x16x256x256_g4", 1, 16, 256 * 256, 4, "bf16"),
+          group_norm("gn_bf16_16x512x64x64_g32", 16, 512, 64 * 64, 32, "bf16"),
+          group_norm("gn_bf16_64x64x8192_g8", 64, 64, 8192, 8, "bf16"),
+          group_norm("gn_f16_1x16x256x256_g4_ones", 1, 16, 256 * 256, 4, "f16",
+                     dy_dist=("const", 1.0, 0.0), gamma_dist=("const", 1.0, 0.0),
+                     beta_dist=("const", 0.0, 0.0)),
+          group_norm("gn_bf16_2x64x32x32_g8_offset16", 2, 64, 32 * 32, 8, "bf16",
+                     x_dist=("normal", 16.0, 1.0))]
     return {w.name: w for w in ws}
