@@ -597,16 +597,15 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
             "timing": "wall clock over steps, synchronised at both ends"}
 
 
-def sources_hash() -> str:
-    """First 16 hex digits of the SHA-256 of the CUDA sources (file names and
-    contents, sorted), to tell whether committed counters still describe
-    the kernels being run."""
-    import glob
+def sources_hash(files) -> str:
+    """First 16 hex digits of the SHA-256 of the named CUDA sources (file
+    names and contents, in the given order), to tell whether committed
+    counters still describe the kernels being run."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "bwd_rms_norm_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for name in files:
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "bwd_rms_norm_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -615,14 +614,14 @@ def load_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary
     (profiles/traffic.json), or {} when it does not cover this workload or
     was taken on kernels other than the ones built from the current
-    sources."""
+    sources (the entry lists the source files its kernels come from)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             data = json.load(f).get(workload, {})
+        if data.get("sources_sha256_16") != sources_hash(data.get("sources", [])):
+            return {}
     except (OSError, ValueError):
-        return {}
-    if data.get("sources_sha256_16") != sources_hash():
         return {}
     return data
 

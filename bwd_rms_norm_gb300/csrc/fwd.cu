@@ -254,14 +254,16 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
 }  // namespace
 
 // Kernel choice by row width (measured on GB300 with the workloads of the
-// tests): rows of up to 16 KB run the register kernels (a row per CTA, 8
-// CTAs per SM in flight); wider rows run the staged TMA pipeline where its
-// ring and registers hold them, else the register kernels, and rows too wide
-// for those are split over a thread-block cluster.
+// tests, as forward+backward steps): rows over 4 KB run the staged TMA
+// pipeline where its ring and registers hold them -- one persistent CTA per
+// SM hands the SMs to the next kernel with less turnover than one CTA per
+// row, which made whole steps 2-9% faster although the forward alone is up
+// to 9% slower on the widest rows -- and rows up to 4 KB run the register
+// kernels.  Rows too wide for both are split over a thread-block cluster.
 cudaError_t launch_fwd(int dtype, const FwdArgs& a, cudaStream_t s, int* launches) {
   cudaError_t e = cudaSuccess;
   const int row_bytes = a.hidden * (dtype == 0 ? 4 : 2);
-  if (row_bytes > 16 * 1024 && try_launch_fwd_tma(dtype, a, s, &e)) {
+  if (row_bytes > 4 * 1024 && try_launch_fwd_tma(dtype, a, s, &e)) {
     if (e == cudaSuccess) *launches += 1;
     return e;
   }

@@ -165,6 +165,8 @@ struct GnArgs {
 };
 
 cudaError_t launch_gn_fwd(int dtype, const GnArgs& a, cudaStream_t s);
+// Bounded-wait timeouts counted by the GroupNorm kernels (group_norm.cu).
+cudaError_t read_gn_wait_timeouts(unsigned int* out);
 cudaError_t launch_gn_bwd(int dtype, const GnArgs& a, cudaStream_t s, int* launches);
 
 // Device properties, cached per device.

@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "mbar.cuh"
 #include "rms_norm.h"
 
 namespace rmsn {
@@ -47,104 +48,19 @@ namespace {
 
 __device__ unsigned int g_wait_timeouts;
 
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // ~1 s
 constexpr int kMaxStages = 32;
 constexpr int kMaxThreads = 1024;
 constexpr int kMaxReducers = 12;
 // Dynamic shared memory for the ring (and the backward's fp32 gain row).
 constexpr int kRingBudget = 200 * 1024;
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// As mbar_try_wait, but the thread may sleep until the phase completes or
-// about `hint_ns` pass, so that waiting warps leave the issue slots to the
-// warps that have work.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
-                                                    uint32_t hint_ns) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return done != 0;
-}
-
-// 1D bulk copy global -> this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Wait for phase `parity` of `bar`.  Returns false if the CTA is aborting or
-// the wait ran out (which starts the abort).
+// Bounded waits counted in this file's timeout counter.
 __device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
-    if (*abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      atomicAdd(&g_wait_timeouts, 1u);
-      return false;
-    }
-  }
+  return wait_phase_counted(bar, parity, abort, &g_wait_timeouts);
 }
 
-// Bounded wait that ignores the abort flag: used to drain copies in flight.
 __device__ void drain_phase(uint64_t* bar, uint32_t parity) {
-  const unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > kWaitLimitNs) {
-      atomicAdd(&g_wait_timeouts, 1u);
-      return;
-    }
-  }
+  drain_phase_counted(bar, parity, &g_wait_timeouts);
 }
 
 // Barriers and per-stage values of the pipeline (static shared memory).
@@ -1037,7 +953,11 @@ bool try_launch_ln_bwd_tma(int dtype, const LnBwdArgs& a, cudaStream_t s, cudaEr
 }
 
 cudaError_t read_wait_timeouts(unsigned int* out) {
-  return cudaMemcpyFromSymbol(out, g_wait_timeouts, sizeof(unsigned int));
+  unsigned int mine = 0, other = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&mine, g_wait_timeouts, sizeof(unsigned int));
+  if (e == cudaSuccess) e = read_gn_wait_timeouts(&other);
+  *out = mine + other;
+  return e;
 }
 
 }  // namespace rmsn
