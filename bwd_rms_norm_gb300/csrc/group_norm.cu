@@ -344,8 +344,10 @@ __global__ void __launch_bounds__(256) gn_bwd_scalar(
 //
 //   producer (warp 0, one thread)  streams the slices of the coming groups
 //       into a ring of shared-memory stages with 1D bulk copies;   -> full[s]
-//   reducers (warps 1..3)  reducer d takes the CTA's groups d, d + 3, ...:
-//       the slice sums, then one pair per group exchanged with the cluster
+//   reducers (three teams of kGnTeamWarps warps)  team d takes the CTA's
+//       groups d, d + 3, ...: its warps split the slice sums (combined at a
+//       team named barrier), then the team's first warp exchanges one pair
+//       per group with the cluster
 //       through distributed shared memory (the reducer stores its pair into
 //       every peer's slot for that reducer and arrives on the peer's
 //       exchange mbarrier), then the group's statistics;        -> red[s]
@@ -373,9 +375,9 @@ __global__ void __launch_bounds__(256) gn_bwd_scalar(
 __device__ unsigned int g_gn_wait_timeouts;
 
 constexpr int kGnStages = 15;
-constexpr int kGnReducers = 3;
-constexpr int kGnAppliersMax = 13;
-constexpr int kGnThreadsMax = 32 * (1 + kGnReducers + kGnAppliersMax);
+constexpr int kGnReducers = 3;      // reducer teams (each takes every third group)
+constexpr int kGnTeamMax = 4;       // warps a team
+constexpr int kGnThreadsMax = 544;  // 17 warps: producer, 3 teams, appliers
 constexpr int kGnSmem = 220 * 1024;  // dynamic shared memory a CTA
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -386,9 +388,41 @@ struct GnPipe {
   float2 stat[kGnStages];      // forward (mean, rstd); backward (c1, c2)
   uint64_t xbar[kGnReducers][2];            // a reducer's pairs arrived
   float2 xch[kGnReducers][2][kMaxCluster];  // ... by sender rank
+  float2 tred[kGnReducers][2][kGnTeamMax];  // team-warp partial sums
   float2 wsum[32];             // applier-warp channel sums (backward)
   int abort;
 };
+
+// Team barrier (named barrier 2 + team over its 32 * tw threads) that also
+// tells whether `ok` held in every warp of the team.
+__device__ __forceinline__ bool team_all(bool ok, int team, int nthreads) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(2 + team), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// The pair (a, b) summed over the warps of a team (each warp passes its own
+// warp total), the same value and order in every lane; `par` alternates.
+__device__ __forceinline__ float2 team_sum2(GnPipe& pp, float2 mine, int team, int tw, int ntw,
+                                            int& par, int lane) {
+  float2* slot = pp.tred[team][par];
+  par ^= 1;
+  if (lane == 0) slot[tw] = mine;
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + team), "r"(32 * ntw) : "memory");
+  float2 t = make_float2(0.f, 0.f);
+  for (int w = 0; w < ntw; ++w) {
+    t.x += slot[w].x;
+    t.y += slot[w].y;
+  }
+  return t;
+}
 
 __device__ bool gn_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   return wait_phase_counted(bar, parity, abort, &g_gn_wait_timeouts);
@@ -544,12 +578,12 @@ template <typename T>
 __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_fwd_pipe(
     const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
     T* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd, int64_t ngroups,
-    int M, int spv, int Cg, int G, float eps, int csize, int stages, int nv) {
+    int M, int spv, int Cg, int G, float eps, int csize, int stages, int nv, int ntw) {
   constexpr int E = Traits<T>::kVec;
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ GnPipe pp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int napp = blockDim.x - 32 * (1 + kGnReducers);
+  const int napp = blockDim.x - 32 * (1 + kGnReducers * ntw);
   const uint32_t rank = csize > 1 ? cta_rank() : 0u;
   const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
   const int64_t g0 = cid * ngroups / ncl;
@@ -568,30 +602,36 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_fwd_pipe(
       gn_produce<1>(pp, ring, stages, sb, src, g0, count, (int64_t)M * sizeof(T),
                     (int64_t)vbase * 16, abort);
     }
-  } else if (warp <= kGnReducers) {
-    const int d = warp - 1;
+  } else if (warp <= kGnReducers * ntw) {
+    // reducer team d of ntw warps: warp tw takes vectors tw*32 + lane,
+    // then every 32*ntw-th; warp 0 of the team exchanges and publishes
+    const int d = (warp - 1) / ntw, tw = (warp - 1) % ntw;
+    const int first = tw * 32 + lane, step = 32 * ntw;
     const float len = (float)(nv * E);
-    int stage = d, par = 0;
+    int stage = d, par = 0, tpar = 0;
     uint32_t ph = 0, xph0 = 0, xph1 = 0;
+    bool prev_ok = true;  // warp 0's last exchange
     for (int i = d; i < count; i += kGnReducers) {
       const int64_t grp = g0 + i;
-      if (!__all_sync(kFull, gn_wait(&pp.full[stage], ph, abort))) break;
+      const bool ok = __all_sync(kFull, gn_wait(&pp.full[stage], ph, abort)) && prev_ok;
+      if (!team_all(ok, d, 32 * ntw)) break;
       const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)stage * sb);
       float part[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) part[e] = 0.f;
 #pragma unroll 4
-      for (int v = lane; v < nv; v += 32) {
+      for (int v = first; v < nv; v += step) {
         float f[E];
         unpack<T>(st[v], f);
 #pragma unroll
         for (int e = 0; e < E; ++e) part[e] += f[e];
       }
-      const float ms = lane_total<E>(part) / len;  // slice mean
+      const float ms =
+          team_sum2(pp, make_float2(lane_total<E>(part), 0.f), d, tw, ntw, tpar, lane).x / len;
 #pragma unroll
       for (int e = 0; e < E; ++e) part[e] = 0.f;
 #pragma unroll 4
-      for (int v = lane; v < nv; v += 32) {
+      for (int v = first; v < nv; v += step) {
         float f[E];
         unpack<T>(st[v], f);
 #pragma unroll
@@ -600,32 +640,36 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_fwd_pipe(
           part[e] = fmaf(c, c, part[e]);
         }
       }
-      const float Q = lane_total<E>(part);
-      float mu = ms, m2 = Q;
-      if (csize > 1) {
-        if (!exchange(pp, d, par, par ? xph1 : xph0, make_float2(ms, Q), rank, csize, lane,
-                      abort))
-          break;
-        if (par) xph1 ^= 1u; else xph0 ^= 1u;
-        float sm = 0.f;
-        for (int r = 0; r < csize; ++r) sm += pp.xch[d][par][r].x;
-        mu = sm / (float)csize;
-        m2 = 0.f;
-        for (int r = 0; r < csize; ++r) {
-          const float c = pp.xch[d][par][r].x - mu;
-          m2 += fmaf(len * c, c, pp.xch[d][par][r].y);
+      const float Q =
+          team_sum2(pp, make_float2(lane_total<E>(part), 0.f), d, tw, ntw, tpar, lane).x;
+      if (tw == 0) {
+        float mu = ms, m2 = Q;
+        if (csize > 1) {
+          prev_ok = exchange(pp, d, par, par ? xph1 : xph0, make_float2(ms, Q), rank, csize,
+                             lane, abort);
+          if (prev_ok) {
+            if (par) xph1 ^= 1u; else xph0 ^= 1u;
+            float sm = 0.f;
+            for (int r = 0; r < csize; ++r) sm += pp.xch[d][par][r].x;
+            mu = sm / (float)csize;
+            m2 = 0.f;
+            for (int r = 0; r < csize; ++r) {
+              const float c = pp.xch[d][par][r].x - mu;
+              m2 += fmaf(len * c, c, pp.xch[d][par][r].y);
+            }
+            par ^= 1;
+          }
         }
-        par ^= 1;
-      }
-      const float rs = rstd_of(m2 / (float)M, eps);
-      if (lane == 0) {
-        pp.stat[stage] = make_float2(mu, rs);
-        if (rank == 0) {
-          mean[grp] = mu;
-          rstd[grp] = rs;
+        if (prev_ok && lane == 0) {
+          const float rs = rstd_of(m2 / (float)M, eps);
+          pp.stat[stage] = make_float2(mu, rs);
+          if (rank == 0) {
+            mean[grp] = mu;
+            rstd[grp] = rs;
+          }
+          mbar_arrive(&pp.red[stage]);
+          mbar_arrive(&pp.empty[stage]);
         }
-        mbar_arrive(&pp.red[stage]);
-        mbar_arrive(&pp.empty[stage]);
       }
       stage += kGnReducers;
       if (stage >= stages) {
@@ -634,7 +678,7 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_fwd_pipe(
       }
     }
   } else {
-    const int a = threadIdx.x - 32 * (1 + kGnReducers);
+    const int a = threadIdx.x - 32 * (1 + kGnReducers * ntw);
     int stage = 0;
     uint32_t ph = 0;
     for (int i = 0; i < count; ++i) {
@@ -674,12 +718,12 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ mean, const float* __restrict__ rstd, T* __restrict__ dx,
     float* __restrict__ partial, int64_t ngroups, int M, int spv, int Cg, int G, int C,
-    int csize, int stages, int nv) {
+    int csize, int stages, int nv, int ntw) {
   constexpr int E = Traits<T>::kVec;
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ GnPipe pp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int napp = blockDim.x - 32 * (1 + kGnReducers);
+  const int napp = blockDim.x - 32 * (1 + kGnReducers * ntw);
   const uint32_t rank = csize > 1 ? cta_rank() : 0u;
   const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
   const int64_t g0 = cid * ngroups / ncl;
@@ -700,23 +744,26 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
       gn_produce<2>(pp, ring, stages, sb, src, g0, count, (int64_t)M * sizeof(T),
                     (int64_t)vbase * 16, abort);
     }
-  } else if (warp <= kGnReducers) {
-    const int d = warp - 1;
-    int stage = d, par = 0;
+  } else if (warp <= kGnReducers * ntw) {
+    const int d = (warp - 1) / ntw, tw = (warp - 1) % ntw;
+    const int first = tw * 32 + lane, step = 32 * ntw;
+    int stage = d, par = 0, tpar = 0;
     uint32_t ph = 0, xph0 = 0, xph1 = 0;
+    bool prev_ok = true;
     for (int i = d; i < count; i += kGnReducers) {
       const int64_t grp = g0 + i;
       const float mu = __ldg(mean + grp), rs = __ldg(rstd + grp);
       const int cbase = (int)(grp % G) * Cg;
-      if (!__all_sync(kFull, gn_wait(&pp.full[stage], ph, abort))) break;
+      const bool ok = __all_sync(kFull, gn_wait(&pp.full[stage], ph, abort)) && prev_ok;
+      if (!team_all(ok, d, 32 * ntw)) break;
       const uint4* sx = reinterpret_cast<const uint4*>(ring + (size_t)stage * 2 * sb);
       const uint4* sd = sx + nv;
       float p1[E], p2[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) p1[e] = p2[e] = 0.f;
-      ChanWalk cw(vbase + lane, 32, spv);
+      ChanWalk cw(vbase + first, step, spv);
 #pragma unroll 2
-      for (int v = lane; v < nv; v += 32, cw.next()) {
+      for (int v = first; v < nv; v += step, cw.next()) {
         const float w = Traits<T>::to_f(gamma[cbase + cw.q]);
         float xf[E], df[E];
         unpack<T>(sx[v], xf);
@@ -728,21 +775,26 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
           p2[e] = fmaf(gd, xf[e] - mu, p2[e]);
         }
       }
-      float2 t = make_float2(lane_total<E>(p1), lane_total<E>(p2));
-      if (csize > 1) {
-        if (!exchange(pp, d, par, par ? xph1 : xph0, t, rank, csize, lane, abort)) break;
-        if (par) xph1 ^= 1u; else xph0 ^= 1u;
-        t = make_float2(0.f, 0.f);
-        for (int r = 0; r < csize; ++r) {
-          t.x += pp.xch[d][par][r].x;
-          t.y += pp.xch[d][par][r].y;
+      float2 t = team_sum2(pp, make_float2(lane_total<E>(p1), lane_total<E>(p2)), d, tw, ntw,
+                           tpar, lane);
+      if (tw == 0) {
+        if (csize > 1) {
+          prev_ok = exchange(pp, d, par, par ? xph1 : xph0, t, rank, csize, lane, abort);
+          if (prev_ok) {
+            if (par) xph1 ^= 1u; else xph0 ^= 1u;
+            t = make_float2(0.f, 0.f);
+            for (int r = 0; r < csize; ++r) {
+              t.x += pp.xch[d][par][r].x;
+              t.y += pp.xch[d][par][r].y;
+            }
+            par ^= 1;
+          }
         }
-        par ^= 1;
-      }
-      if (lane == 0) {
-        pp.stat[stage] = make_float2(t.x / (float)M, t.y * rs / (float)M);
-        mbar_arrive(&pp.red[stage]);
-        mbar_arrive(&pp.empty[stage]);
+        if (prev_ok && lane == 0) {
+          pp.stat[stage] = make_float2(t.x / (float)M, t.y * rs / (float)M);
+          mbar_arrive(&pp.red[stage]);
+          mbar_arrive(&pp.empty[stage]);
+        }
       }
       stage += kGnReducers;
       if (stage >= stages) {
@@ -751,7 +803,7 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
       }
     }
   } else {
-    const int a = threadIdx.x - 32 * (1 + kGnReducers);
+    const int a = threadIdx.x - 32 * (1 + kGnReducers * ntw);
     const int cwi = a >> 5, ncw = napp >> 5;
     const int c_lo = vbase / spv, c_hi = (vbase + nv - 1) / spv;
     const int nch = c_hi - c_lo + 1;
@@ -856,31 +908,44 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
 }
 
 // Pipeline shape: the smallest cluster (1..16 CTAs) whose slices leave at
-// least three ring stages (a multiple of the reducer count) in kGnSmem (the
-// backward also keeps a float2 per slice vector); false when none does.
+// least min_stages ring stages (a multiple of the reducer count) in kGnSmem
+// (the backward also keeps a float2 per slice vector); false when none
+// does.
 struct PipeShape {
   int csize, stages, nv, threads;
   size_t smem;
+  int ntw;  // warps a reducer team
 };
 
-bool pick_pipe(int nvec, bool bwd, PipeShape* ps) {
+// Warps a reducer team (measured on GB300: 2 beat 1, 3 and 4).
+constexpr int kGnTeamWarps = 2;
+
+bool pick_pipe_min(int nvec, bool bwd, int min_stages, PipeShape* ps) {
   for (int k = 1; k <= kMaxCluster; k *= 2) {
     if (nvec % k) continue;
     const int nv = nvec / k;
     const size_t sb = (size_t)nv * 16;
     const size_t per = bwd ? 2 * sb : sb;
     const size_t extra = bwd ? (size_t)nv * sizeof(float2) : 0;
-    if (extra + 3 * per > (size_t)kGnSmem) continue;
+    if (extra + (size_t)min_stages * per > (size_t)kGnSmem) continue;
     int st = (int)(((size_t)kGnSmem - extra) / per);
     if (st > kGnStages) st = kGnStages;
     st -= st % kGnReducers;
+    const int ntw = kGnTeamWarps;
     int apps = (nv + 31) / 32;
-    if (apps > kGnAppliersMax) apps = kGnAppliersMax;
-    *ps = PipeShape{k, st, nv, 32 * (1 + kGnReducers + apps), (size_t)st * per + extra};
+    const int max_apps = kGnThreadsMax / 32 - 1 - kGnReducers * ntw;
+    if (apps > max_apps) apps = max_apps;
+    *ps = PipeShape{k, st, nv, 32 * (1 + kGnReducers * ntw + apps), (size_t)st * per + extra, ntw};
     return true;
   }
   return false;
 }
+
+// The smallest cluster with three stages: measured on GB300, larger
+// clusters with deeper rings are slower (fewer resident clusters, costlier
+// exchanges), e.g. the (16, 512, 64, 64) backward takes 101 us with six
+// stages in clusters of 8 against 63 us with three in clusters of 4.
+bool pick_pipe(int nvec, bool bwd, PipeShape* ps) { return pick_pipe_min(nvec, bwd, 3, ps); }
 
 // Whether clusters of `csize` CTAs of `block` threads of `kern` can be
 // resident on the current device (some sizes above 8 cannot), cached.
@@ -1023,7 +1088,8 @@ cudaError_t gn_fwd_t(const GnArgs& a, cudaStream_t s) {
         const int64_t ncl = active < groups ? active : groups;
         return launch_kernel(kern, dim3((unsigned)(ncl * ps.csize)), dim3(ps.threads), ps.smem,
                              s, ps.csize, x, g, b, y, a.mean, a.rstd, groups, M,
-                             a.spatial / E, Cg, a.groups, a.eps, ps.csize, ps.stages, ps.nv);
+                             a.spatial / E, Cg, a.groups, a.eps, ps.csize, ps.stages, ps.nv,
+                             ps.ntw);
       }
     }
     // halve the cluster while it cannot be resident, as long as a CTA
@@ -1067,7 +1133,8 @@ cudaError_t gn_bwd_t(const GnArgs& a, cudaStream_t s, int* launches) {
       csize = ps.csize;
       e = launch_kernel(kern, dim3((unsigned)(ncl * ps.csize)), dim3(ps.threads), ps.smem, s,
                         ps.csize, dy, x, g, a.mean, a.rstd, dx, a.partial, groups, M,
-                        a.spatial / E, Cg, a.groups, a.channels, ps.csize, ps.stages, ps.nv);
+                        a.spatial / E, Cg, a.groups, a.channels, ps.csize, ps.stages, ps.nv,
+                        ps.ntw);
     }
   }
   if (csize == 0 && a.vec_ok) {
