@@ -160,6 +160,26 @@ __device__ __forceinline__ float pairwise(float (&p)[E]) {
   return p[0];
 }
 
+// The fp32 gains (gamma + off) in shared memory for the reducers, one
+// 16-byte vector of gamma per load.  Vector v's E gains are stored as E/4
+// float4 in E/4 planes of nvec float4 each (plane q holds elements 4q..4q+3
+// of every vector), so that a warp reading the planes of 32 consecutive
+// vectors reads 512 contiguous bytes: no bank conflicts.
+template <typename T>
+__device__ __forceinline__ void stage_gains(float* gain, const T* __restrict__ gamma, int nvec,
+                                            float off, int t, int nthreads) {
+  constexpr int E = Traits<T>::kVec;
+  float4* g4 = reinterpret_cast<float4*>(gain);
+  for (int v = t; v < nvec; v += nthreads) {
+    float f[E];
+    unpack<T>(ld_shared_ro(gamma + (int64_t)v * E), f);
+#pragma unroll
+    for (int e = 0; e < E; e += 4)
+      g4[(e / 4) * nvec + v] = make_float4(f[e] + off, f[e + 1] + off, f[e + 2] + off,
+                                           f[e + 3] + off);
+  }
+}
+
 // Forward.  Reducer: sum of squares of its row, rstd, written to global and
 // to the stage's slot.  Appliers: y = round((x * rstd) * gain) (or the
 // round-twice store) for their vectors of every row.
@@ -312,14 +332,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   }
 
   if (warp <= reducers) {
-    // The reducers stage the fp32 gains.  Vector v's E gains are stored as
-    // E/4 float4 in E/4 planes of nvec float4 each (plane q holds elements
-    // 4q..4q+3 of every vector), so that a warp reading the planes of 32
-    // consecutive vectors reads 512 contiguous bytes: no bank conflicts.
-    for (int j = threadIdx.x - 32; j < hidden; j += 32 * reducers) {
-      const int v = j / E, e = j % E;
-      gain[((e / 4) * nvec + v) * 4 + (e % 4)] = Traits<T>::to_f(gamma[j]) + off;
-    }
+    // The reducers stage the fp32 gains (plane-split, see stage_gains).
+    stage_gains<T>(gain, gamma, nvec, off, threadIdx.x - 32, 32 * reducers);
     asm volatile("bar.sync 1, %0;" ::"r"(32 * reducers) : "memory");
     const float4* g4 = reinterpret_cast<const float4*>(gain);
     const int d = warp - 1;
@@ -581,10 +595,7 @@ __global__ void __launch_bounds__(VPT == 2 ? kLnBwd2Threads : kMaxThreads, 1) ln
   }
 
   if (warp <= reducers) {
-    for (int j = threadIdx.x - 32; j < hidden; j += 32 * reducers) {
-      const int v = j / E, e = j % E;
-      gain[((e / 4) * nvec + v) * 4 + (e % 4)] = Traits<T>::to_f(gamma[j]);
-    }
+    stage_gains<T>(gain, gamma, nvec, 0.f, threadIdx.x - 32, 32 * reducers);
     asm volatile("bar.sync 1, %0;" ::"r"(32 * reducers) : "memory");
     const float4* g4 = reinterpret_cast<const float4*>(gain);
     const int d = warp - 1;
