@@ -709,6 +709,159 @@ __global__ void __launch_bounds__(VPT == 2 ? kLnBwd2Threads : kMaxThreads, 1) ln
   }
 }
 
+// Backward for wide rows (2048 vectors: 16384 16-bit or 8192 fp32 elements)
+// that bwd_tma cannot hold: its fp32 gain copy and two ring stages would
+// fill shared memory, and two vectors per applier do not cover the row.
+// Here the reducers read the gains through L1 (16-byte loads, every row)
+// instead of a shared-memory copy, which leaves room for three stages, and
+// each applier owns four vectors with its gains kept packed in registers
+// (widened at each use) next to its fp32 dw accumulators; the block is
+// limited to 736 threads, which leaves 88 registers a thread.  A row's dot
+// is split over a team of kWideTeam reducer warps (three teams, each taking
+// every third row) that meet at their own named barrier.
+constexpr int kWideThreads = 736;
+constexpr int kWideTeam = 2;  // warps a reducer team (three teams)
+
+template <typename T>
+__global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
+    const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
+    const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
+    int64_t rows, int hidden, float off, int stages, int reducers) {
+  constexpr int E = Traits<T>::kVec;
+  constexpr int VPT = 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Pipe pipe;
+  const int row_bytes = hidden * (int)sizeof(T);
+  const int stride = (2 * row_bytes + 127) / 128 * 128;
+  unsigned char* ring = smem;
+  const int appliers = blockDim.x - 32 * (1 + reducers * kWideTeam);
+  const Rows rw = cta_rows(rows);
+  const int n = rw.n;
+  init_pipe(pipe, stages, appliers / 32);
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  volatile int* abort = &pipe.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = hidden / E;
+  const int doff = row_bytes / 16;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const void* const src[2] = {x, dy};
+      produce<2>(pipe, ring, stride, stages, src, rw, (uint32_t)row_bytes, abort);
+    }
+    return;
+  }
+
+  if (warp <= reducers * kWideTeam) {
+    __shared__ float tred[3][2][kWideTeam];
+    const int d = (warp - 1) / kWideTeam, tw = (warp - 1) % kWideTeam;
+    const int nthr = 32 * kWideTeam;
+    int tpar = 0;
+    RingPos pos{0, 0u};
+    pos.advance(d, stages);
+    for (int i = d; i < n; i += reducers) {
+      const float rs = __ldg(rstd + rw.row(i));
+      // the team decides together: a named barrier that ANDs every warp's wait
+      const bool ok = __all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort));
+      uint32_t all_ok;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\t"
+          "setp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.and.pred q, %2, %3, p;\n\t"
+          "selp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(all_ok)
+          : "r"((uint32_t)ok), "r"(2 + d), "r"(nthr)
+          : "memory");
+      if (!all_ok) return;
+      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+      float part[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) part[e] = 0.f;
+      for (int v = tw * 32 + lane; v < nvec; v += nthr) {
+        float xf[E], df[E], gf[E];
+        unpack<T>(st[v], xf);
+        unpack<T>(st[doff + v], df);
+        unpack<T>(ld_shared_ro(gamma + (int64_t)v * E), gf);
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[e] = fmaf(df[e] * (gf[e] + off), xf[e], part[e]);
+      }
+      const float wdot = warp_sum(pairwise<E>(part));
+      float* slot = tred[d][tpar];
+      tpar ^= 1;
+      if (lane == 0) slot[tw] = wdot;
+      asm volatile("bar.sync %0, %1;" ::"r"(2 + d), "r"(nthr) : "memory");
+      if (tw == 0 && lane == 0) {
+        float dot = 0.f;
+        for (int w = 0; w < kWideTeam; ++w) dot += slot[w];
+        pipe.stat[pos.stage] = dot * rs / (float)hidden;
+        mbar_arrive(&pipe.red[pos.stage]);
+        mbar_arrive(&pipe.empty[pos.stage]);
+      }
+      pos.advance(reducers, stages);
+    }
+    return;
+  }
+
+  const int a = threadIdx.x - 32 * (1 + reducers * kWideTeam);
+  uint4 gp[VPT];
+  float acc[VPT][E];
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = a + j * appliers;
+    gp[j] = v < nvec ? ld_shared_ro(gamma + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[j][e] = 0.f;
+  }
+  RingPos pos{0, 0u};
+  float rs_next = n > 0 ? __ldg(rstd + rw.row(0)) : 0.f;
+  for (int i = 0; i < n; ++i) {
+    const float rs = rs_next;
+    if (i + 1 < n) rs_next = __ldg(rstd + rw.row(i + 1));
+    bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
+    ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const float c = pipe.stat[pos.stage];
+    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+    T* dxr = dx + rw.row(i) * hidden;
+    // widen the packed gains at each use rather than holding them widened
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) opaque(gp[j]);
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = a + j * appliers;
+      if (v < nvec) {
+        float xf[E], df[E], gf[E], o[E];
+        unpack<T>(st[v], xf);
+        unpack<T>(st[doff + v], df);
+        unpack<T>(gp[j], gf);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float xh = xf[e] * rs;
+          acc[j][e] = fmaf(df[e], xh, acc[j][e]);
+          o[e] = fmaf(-xh, c, df[e] * (gf[e] + off)) * rs;
+        }
+        st_vec(dxr + (int64_t)v * E, pack<T>(o));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
+    pos.advance(1, stages);
+  }
+  float* pr = partial + (int64_t)blockIdx.x * hidden;
+#pragma unroll
+  for (int j = 0; j < VPT; ++j) {
+    const int v = a + j * appliers;
+    if (v < nvec) {
+#pragma unroll
+      for (int e = 0; e < E; e += 4)
+        *reinterpret_cast<float4*>(pr + (int64_t)v * E + e) =
+            make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
+    }
+  }
+}
+
 std::mutex g_attr_mutex;
 struct AttrEntry {
   const void* func;
@@ -828,6 +981,31 @@ cudaError_t launch_bwd_tma_v(const BwdArgs& a, int appliers, int stages, int red
                        a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers);
 }
 
+// The wide-row backward: three stages without a shared gain copy and four
+// vectors per applier within kWideThreads threads; false when that does not
+// fit either.
+template <typename T>
+bool try_bwd_wide_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+  constexpr int E = Traits<T>::kVec;
+  const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  const int stages = kRingBudget / stride >= 3 ? 3 : 0, reducers = 3;
+  if (stages < 3) return false;
+  int appliers = 0;
+  if (pick_vpt(a.hidden / E, kWideThreads - 32 * (1 + reducers * kWideTeam), 4, &appliers) != 4)
+    return false;
+  const int grid = grid_for(a.rows, a.max_partials, err);
+  if (*err != cudaSuccess) return true;
+  *nparts = grid;
+  auto kern = bwd_tma_wide<T>;
+  if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
+  *err = launch_kernel(kern, dim3(grid), dim3(32 * (1 + reducers * kWideTeam) + appliers),
+                       (size_t)stages * stride, s, 1, static_cast<const T*>(a.dy),
+                       static_cast<const T*>(a.x), static_cast<const T*>(a.gamma), a.rstd,
+                       static_cast<T*>(a.dx), a.partial, a.rows, a.hidden,
+                       a.offset ? 1.f : 0.f, stages, reducers);
+  return true;
+}
+
 template <typename T>
 bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
   constexpr int E = Traits<T>::kVec;
@@ -835,11 +1013,12 @@ bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* npar
   const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
   int stages = 0, reducers = 0;
   split_stages((kRingBudget - gain_bytes) / stride, &stages, &reducers);
-  if (stages < 3) return false;
   int appliers = 0;
   // at most 2 vectors per applier: gains and dw accumulators in registers
-  const int vpt = pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 2, &appliers);
-  if (vpt == 0) return false;
+  const int vpt = stages < 3 ? 0
+                             : pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 2,
+                                        &appliers);
+  if (vpt == 0) return try_bwd_wide_t<T>(a, s, err, nparts);
   const int grid = grid_for(a.rows, a.max_partials, err);
   if (*err != cudaSuccess) return true;
   *nparts = grid;

@@ -102,6 +102,9 @@ SHAPES = [
     (3, 16392, "bf16"), (2, 32768, "f32"), (2, 65536, "bf16"), (2, 65536, "f32"),
     (2, 65536, "f16"), (300, 4096, "bf16"), (151, 2048, "f16"), (153, 512, "f32"),
     (1, 32768, "f16"), (33, 3072, "bf16"), (2, 7, "f16"),
+    # the staged backward for 2048-vector rows (gains read through L1, four
+    # vectors per applier): ragged row counts over the 152-CTA grid
+    (1000, 16384, "f16"), (157, 16384, "bf16"), (301, 8192, "f32"),
 ]
 
 
