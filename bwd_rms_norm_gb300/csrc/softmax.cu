@@ -261,6 +261,40 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) sm_bwd_cta_row(
   }
 }
 
+// Persistent backward for rows of one vector a thread: the CTA
+// walks a contiguous range of rows and loads the next row's y and dy while
+// the current row's dot is reduced, so loads stay in flight across the
+// CTA reduction.
+template <typename T>
+__global__ void __launch_bounds__(1024) sm_bwd_rows(const T* __restrict__ dy,
+                                                   const T* __restrict__ y,
+                                                   T* __restrict__ dx, int64_t rows, int cols) {
+  constexpr int E = Traits<T>::kVec;
+  __shared__ float red[64];
+  const int nvec = cols / E;
+  const int v = threadIdx.x;
+  const bool in = v < nvec;
+  const int64_t r0 = (int64_t)blockIdx.x * rows / gridDim.x;
+  const int64_t r1 = (int64_t)(blockIdx.x + 1) * rows / gridDim.x;
+  pdl_trigger();
+  pdl_wait();
+  auto load = [&](int64_t r, uint4& yb, uint4& db) {
+    yb = in ? ld_stream(y + r * cols + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+    db = in ? ld_stream(dy + r * cols + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+  };
+  uint4 yc[1], dc[1], yn, dn;
+  if (r0 < r1) load(r0, yc[0], dc[0]);
+  int parity = 0;
+  for (int64_t r = r0; r < r1; ++r) {
+    if (r + 1 < r1) load(r + 1, yn, dn);
+    const float d = block_sum(local_dot<T, 1>(yc, dc), red, parity);
+    parity ^= 1;
+    if (in) st_vec(dx + r * cols + (int64_t)v * E, sm_dx_vec<T>(yc[0], dc[0], d));
+    yc[0] = yn;
+    dc[0] = dn;
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) sm_bwd_scalar(const T* __restrict__ dy,
                                                      const T* __restrict__ y, T* __restrict__ dx,
@@ -355,9 +389,21 @@ cudaError_t sm_bwd_t(const SoftmaxArgs& a, cudaStream_t s) {
   }
   int vpt = 0, tpr = 0;
   if (a.vec_ok) bwd_shape(nvec, &vpt, &tpr);
+  if (vpt == 1 && tpr > 512) {
+    // rows that fill a CTA of more than 512 threads (at most two resident
+    // per SM): persistent CTAs that keep the next row loading, as many as
+    // are resident at once.  Measured on GB300: 6% faster at 8192 bf16
+    // columns, 5% slower at 4096 (four row CTAs per SM overlap already).
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    auto kern = sm_bwd_rows<T>;
+    int64_t g = (int64_t)sm_count(dev) * max_blocks_per_sm((const void*)kern, tpr, 0);
+    if (g > a.rows) g = a.rows;
+    return launch_kernel(kern, dim3((unsigned)g), dim3(tpr), 0, s, 1, dy, y, dx, a.rows, a.cols);
+  }
   const dim3 grid((unsigned)a.rows);
   switch (vpt) {
-    case 1: return launch_kernel(sm_bwd_cta_row<T, 1>, grid, dim3(tpr), 0, s, 1, dy, y, dx, a.cols);
     case 2: return launch_kernel(sm_bwd_cta_row<T, 2>, grid, dim3(tpr), 0, s, 1, dy, y, dx, a.cols);
     case 8: return launch_kernel(sm_bwd_cta_row<T, 8>, grid, dim3(tpr), 0, s, 1, dy, y, dx, a.cols);
     default: return launch_kernel(sm_bwd_scalar<T>, grid, dim3(256), 0, s, 1, dy, y, dx, a.cols);
