@@ -53,6 +53,7 @@ EXPORTED = (
     "rms_norm_status_string",
     "rms_norm_last_cuda_error",
     "rms_norm_last_launch_count",
+    "rms_norm_last_kernels",
     "rms_norm_bwd_noalloc",
     "rms_norm_wait_timeouts",
     "rms_norm_fwd_fp8",
@@ -98,6 +99,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_status_string.restype = ctypes.c_char_p
     lib.rms_norm_last_cuda_error.argtypes = []
     lib.rms_norm_last_cuda_error.restype = I
+    lib.rms_norm_last_kernels.argtypes = [ctypes.POINTER(ctypes.c_char_p), I]
+    lib.rms_norm_last_kernels.restype = I
     lib.rms_norm_last_launch_count.argtypes = []
     lib.rms_norm_last_launch_count.restype = I
     lib.rms_norm_bwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I, I, P]
@@ -140,6 +143,13 @@ def rms_norm_bwd_workspace_size(rows: int, hidden: int, dtype) -> int:
 def last_launch_count() -> int:
     """Kernels enqueued by the last successful call on this thread."""
     return int(load_library().rms_norm_last_launch_count())
+
+
+def last_kernels() -> list:
+    """Symbol names of the kernels the last call on this thread launched."""
+    buf = (ctypes.c_char_p * 4)()
+    n = load_library().rms_norm_last_kernels(buf, 4)
+    return [buf[i].decode() for i in range(max(n, 0))]
 
 
 def wait_timeouts() -> int:

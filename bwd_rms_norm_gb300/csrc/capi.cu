@@ -14,6 +14,7 @@ namespace rmsn {
 namespace {
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_launches = 0;
+thread_local LaunchLog t_launch_log = {{nullptr, nullptr, nullptr, nullptr}, 0};
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -38,6 +39,14 @@ int cuda_fail(cudaError_t e) {
   return RMSN_ERR_CUDA;
 }
 }  // namespace
+
+LaunchLog& launch_log() { return t_launch_log; }
+
+// Start of a C-ABI call: nothing launched yet.
+void begin_call() {
+  t_last_launches = 0;
+  t_launch_log.n = 0;
+}
 
 int sm_count(int device) {
   if (device >= 0 && device < kMaxDevices) {
@@ -84,7 +93,7 @@ int rms_norm_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t
   if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
     return RMSN_ERR_SHAPE;
   if (!(eps >= 0.f) || isinf(eps)) return RMSN_ERR_EPS;
-  t_last_launches = 0;
+  begin_call();
   if (rows == 0) return RMSN_OK;
   if (!x || !gamma || !y || !rstd) return RMSN_ERR_NULL;
 
@@ -117,7 +126,7 @@ int rms_norm_fwd_fp8(const void* x, const void* gamma, const float* scale, void*
   if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
     return RMSN_ERR_SHAPE;
   if (!(eps >= 0.f) || isinf(eps)) return RMSN_ERR_EPS;
-  t_last_launches = 0;
+  begin_call();
   if (rows == 0) return RMSN_OK;
   if (!x || !gamma || !scale || !y || !rstd) return RMSN_ERR_NULL;
   const int s = elem_bytes(dtype);
@@ -157,7 +166,7 @@ int rms_norm_bwd(const void* dy, const void* x, const void* gamma, const float* 
   if (offset != 0 && offset != 1) return RMSN_ERR_ARG;
   if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
     return RMSN_ERR_SHAPE;
-  t_last_launches = 0;
+  begin_call();
   if (!dw) return RMSN_ERR_NULL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (rows == 0) {
@@ -199,7 +208,7 @@ int layer_norm_fwd(const void* x, const void* gamma, const void* beta, void* y, 
   if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
     return RMSN_ERR_SHAPE;
   if (!(eps >= 0.f) || isinf(eps)) return RMSN_ERR_EPS;
-  t_last_launches = 0;
+  begin_call();
   if (rows == 0) return RMSN_OK;
   if (!x || !gamma || !y || !mean || !rstd) return RMSN_ERR_NULL;
   const int s = elem_bytes(dtype);
@@ -233,7 +242,7 @@ int layer_norm_bwd(const void* dy, const void* x, const void* gamma, const float
   if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
   if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
     return RMSN_ERR_SHAPE;
-  t_last_launches = 0;
+  begin_call();
   if (!dgamma) return RMSN_ERR_NULL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (rows == 0) {
@@ -273,7 +282,7 @@ int softmax_fwd(const void* x, void* y, int64_t rows, int64_t cols, int dtype, v
   if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
   if (rows < 0 || rows > RMSN_MAX_ROWS || cols < 1 || cols > RMSN_MAX_HIDDEN)
     return RMSN_ERR_SHAPE;
-  t_last_launches = 0;
+  begin_call();
   if (rows == 0) return RMSN_OK;
   if (!x || !y) return RMSN_ERR_NULL;
   SoftmaxArgs a{};
@@ -293,7 +302,7 @@ int softmax_bwd(const void* dy, const void* y, void* dx, int64_t rows, int64_t c
   if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
   if (rows < 0 || rows > RMSN_MAX_ROWS || cols < 1 || cols > RMSN_MAX_HIDDEN)
     return RMSN_ERR_SHAPE;
-  t_last_launches = 0;
+  begin_call();
   if (rows == 0) return RMSN_OK;
   if (!dy || !y || !dx) return RMSN_ERR_NULL;
   SoftmaxArgs a{};
@@ -327,7 +336,7 @@ int group_norm_fwd(const void* x, const void* gamma, const void* beta, void* y, 
   if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
   if (!gn_shape_ok(n, channels, spatial, groups)) return RMSN_ERR_SHAPE;
   if (!(eps >= 0.f) || isinf(eps)) return RMSN_ERR_EPS;
-  t_last_launches = 0;
+  begin_call();
   if (n == 0) return RMSN_OK;
   if (!x || !gamma || !y || !mean || !rstd) return RMSN_ERR_NULL;
   GnArgs a{};
@@ -363,7 +372,7 @@ int group_norm_bwd(const void* dy, const void* x, const void* gamma, const float
                    void* workspace, size_t workspace_bytes, void* stream) {
   if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
   if (!gn_shape_ok(n, channels, spatial, groups)) return RMSN_ERR_SHAPE;
-  t_last_launches = 0;
+  begin_call();
   if (!dgamma) return RMSN_ERR_NULL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (n == 0) {
@@ -416,5 +425,17 @@ const char* rms_norm_status_string(int status) {
 int rms_norm_last_cuda_error(void) { return t_last_cuda_error; }
 
 int rms_norm_last_launch_count(void) { return t_last_launches; }
+
+int rms_norm_last_kernels(const char** names, int max_names) {
+  if (!names || max_names < 0) return -RMSN_ERR_NULL;
+  const int n = t_launch_log.n < max_names ? t_launch_log.n : max_names;
+  for (int i = 0; i < n; ++i) {
+    if (cudaFuncGetName(&names[i], t_launch_log.kern[i]) != cudaSuccess) {
+      cudaGetLastError();
+      names[i] = "?";
+    }
+  }
+  return n;
+}
 
 }  // extern "C"

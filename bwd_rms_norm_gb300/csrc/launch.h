@@ -57,6 +57,16 @@ bool try_launch_fwd_cluster(int dtype, const FwdArgs& a, cudaStream_t s, cudaErr
 bool try_launch_bwd_cluster(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
                             int* nparts);
 
+// The kernels the current C-ABI call on this thread has launched, in order
+// (the first four), for rms_norm_last_kernels().  capi.cu.
+struct LaunchLog {
+  const void* kern[4];
+  int n;
+};
+LaunchLog& launch_log();
+// Start of a C-ABI call on this thread: clears the launch count and log.
+void begin_call();
+
 // Launch `kern` with programmatic dependent launch allowed (see pdl_wait in
 // common.cuh) and, when `cluster` > 1, thread-block clusters of `cluster`
 // CTAs along x.
@@ -81,7 +91,10 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  LaunchLog& log = launch_log();
+  if (e == cudaSuccess && log.n < 4) log.kern[log.n++] = reinterpret_cast<const void*>(kern);
+  return e;
 }
 
 // out[j] = sum over the nparts rows of the fp32 matrix `partial`

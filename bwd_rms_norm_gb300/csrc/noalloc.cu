@@ -52,6 +52,7 @@ extern "C" int rms_norm_bwd_noalloc(const void* dy, const void* x, const void* g
                                     int64_t hidden, int offset, int dtype, void* stream) {
   using namespace rmsn;
   if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  rmsn::begin_call();
   if (offset != 0 && offset != 1) return RMSN_ERR_ARG;
   if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
     return RMSN_ERR_SHAPE;

@@ -404,6 +404,7 @@ cudaError_t sm_bwd_t(const SoftmaxArgs& a, cudaStream_t s) {
   }
   const dim3 grid((unsigned)a.rows);
   switch (vpt) {
+    case 1: return launch_kernel(sm_bwd_cta_row<T, 1>, grid, dim3(tpr), 0, s, 1, dy, y, dx, a.cols);
     case 2: return launch_kernel(sm_bwd_cta_row<T, 2>, grid, dim3(tpr), 0, s, 1, dy, y, dx, a.cols);
     case 8: return launch_kernel(sm_bwd_cta_row<T, 8>, grid, dim3(tpr), 0, s, 1, dy, y, dx, a.cols);
     default: return launch_kernel(sm_bwd_scalar<T>, grid, dim3(256), 0, s, 1, dy, y, dx, a.cols);

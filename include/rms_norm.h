@@ -251,6 +251,17 @@ int group_norm_bwd(const void* dy, const void* x, const void* gamma,
                    int64_t spatial, int64_t groups, int dtype, void* workspace,
                    size_t workspace_bytes, void* stream);
 
+/*
+ * Introspection: the device kernels that the last call of any entry point
+ * of this library on the calling thread launched, in launch order (at most
+ * four are recorded).  names[i] receives a static, NUL-terminated string
+ * (the kernel's symbol name as the CUDA runtime reports it) for
+ * i < min(count, max_names); the return value is that count, or
+ * -RMSN_ERR_NULL when names is NULL.  A call that launched nothing (rows ==
+ * 0, a validation error) reports 0.  Needs no device work.
+ */
+int rms_norm_last_kernels(const char** names, int max_names);
+
 /* Static, NUL-terminated description of a status code. */
 const char* rms_norm_status_string(int status);
 

@@ -218,3 +218,12 @@ def test_group_norm_validation(lib):
         assert b(**{k: NULL}) == 1, k
     assert b(ws=ctypes.c_void_p(0x1004)) == 5
     assert b(ws_bytes=64) == 6
+
+
+def test_last_kernels_without_launches(lib):
+    """Before any launch on this thread, or after a call rejected on the
+    host, no kernel is reported (no GPU involved)."""
+    names = (ctypes.c_char_p * 4)()
+    assert fwd(lib, dtype=3) == 4
+    assert lib.rms_norm_last_kernels(names, 4) == 0
+    assert lib.rms_norm_last_kernels(None, 4) < 0
