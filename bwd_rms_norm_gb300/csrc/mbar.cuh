@@ -105,4 +105,42 @@ __device__ __forceinline__ void drain_phase_counted(uint64_t* bar, uint32_t pari
   }
 }
 
+// Arrive on the mbarrier at `local_bar`'s address in CTA `peer` of the
+// cluster, releasing this thread's earlier stores at cluster scope.
+__device__ __forceinline__ void mbar_arrive_peer(uint64_t* local_bar, uint32_t peer) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(smem_u32(local_bar)), "r"(peer));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
+               : "memory");
+}
+
+// Bounded wait on an mbarrier that peer CTAs arrive on, with acquire at
+// cluster scope (their stores made before the arrive are visible after it).
+// Returns false if the CTA is aborting or the wait ran out (which starts the
+// abort and counts in *timeouts).
+__device__ __forceinline__ bool wait_cluster_counted(uint64_t* bar, uint32_t parity,
+                                                     volatile int* abort,
+                                                     unsigned int* timeouts) {
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      atomicAdd(timeouts, 1u);
+      return false;
+    }
+  }
+}
+
 }  // namespace rmsn

@@ -38,6 +38,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "cluster.cuh"
 #include "launch.h"
 #include "mbar.cuh"
 #include "rms_norm.h"
@@ -117,10 +118,12 @@ __device__ __forceinline__ void init_pipe(Pipe& p, int stages, int applier_warps
 
 // Producer: issue the copies of the CTA's rows (its i-th row is rw.row(i))
 // into the ring.  NSRC source tensors go to consecutive parts of a stage.
+// Rows are `pitch` bytes apart in global memory; `bytes` of each are copied
+// (a whole row, or the slice a CTA of a cluster owns).
 template <int NSRC>
-__device__ void produce(Pipe& p, unsigned char* ring, int stride, int stages,
-                        const void* const (&src)[NSRC], const Rows& rw, uint32_t row_bytes,
-                        volatile int* abort) {
+__device__ void produce_pitched(Pipe& p, unsigned char* ring, int stride, int stages,
+                                const void* const (&src)[NSRC], const Rows& rw, size_t pitch,
+                                uint32_t bytes, volatile int* abort) {
   RingPos pos{0, 0u};
   int i = 0;
   const int n = rw.n;
@@ -128,11 +131,11 @@ __device__ void produce(Pipe& p, unsigned char* ring, int stride, int stages,
     // the stage's previous use (parity phase ^ 1) must be released first
     if (i >= stages && !wait_phase(&p.empty[pos.stage], pos.phase ^ 1u, abort)) break;
     unsigned char* dst = ring + (size_t)pos.stage * stride;
-    mbar_arrive_expect_tx(&p.full[pos.stage], NSRC * row_bytes);
-    const size_t off = (size_t)rw.row(i) * row_bytes;
+    mbar_arrive_expect_tx(&p.full[pos.stage], NSRC * bytes);
+    const size_t off = (size_t)rw.row(i) * pitch;
 #pragma unroll
     for (int t = 0; t < NSRC; ++t)
-      bulk_load(dst + t * row_bytes, static_cast<const unsigned char*>(src[t]) + off, row_bytes,
+      bulk_load(dst + t * bytes, static_cast<const unsigned char*>(src[t]) + off, bytes,
                 &p.full[pos.stage]);
     pos.advance(1, stages);
   }
@@ -148,6 +151,13 @@ __device__ void produce(Pipe& p, unsigned char* ring, int stride, int stages,
     }
     drain_phase(&p.full[pos.stage], pos.phase);
   }
+}
+
+template <int NSRC>
+__device__ __forceinline__ void produce(Pipe& p, unsigned char* ring, int stride, int stages,
+                                        const void* const (&src)[NSRC], const Rows& rw,
+                                        uint32_t row_bytes, volatile int* abort) {
+  produce_pitched<NSRC>(p, ring, stride, stages, src, rw, row_bytes, row_bytes, abort);
 }
 
 // Sum of per-element partial sums, pairwise.
@@ -981,6 +991,235 @@ cudaError_t launch_bwd_tma_v(const BwdArgs& a, int appliers, int stages, int red
                        a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers);
 }
 
+// Backward for rows of 4096 vectors (32768 16-bit or 16384 fp32 elements)
+// over a cluster of two CTAs: CTA q of the pair stages, reduces and writes
+// columns [q * N/2, (q+1) * N/2) of every row of the pair's contiguous row
+// range, so a ring stage (its halves of x and dy) is 64 KB and three fit.
+// The roles are those of bwd_tma_wide (reducer teams of kWideTeam warps,
+// appliers of four vectors with packed gains); a team's half-row dot is
+// exchanged with the peer CTA through distributed shared memory -- the
+// team's first warp stores it into the peer's slot and arrives on the
+// peer's exchange mbarrier -- and both CTAs add the two halves in rank
+// order.  Exchange slots are double-buffered per team (the peer cannot
+// start the team's row after next before this CTA has read the current
+// one: that row needs this CTA's next half).  Every CTA ends with a cluster
+// barrier so that no CTA exits while its peer may still store into it.
+template <typename T>
+__global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_pair(
+    const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
+    const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
+    int64_t rows, int hidden, float off, int stages, int reducers) {
+  constexpr int E = Traits<T>::kVec;
+  constexpr int VPT = 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Pipe pipe;
+  __shared__ uint64_t xbar[3][2];
+  __shared__ float xch[3][2][2];
+  __shared__ float tred[3][2][kWideTeam];
+  const uint32_t rank = cta_rank();
+  const int half = hidden / 2;               // columns a CTA owns
+  const int half_bytes = half * (int)sizeof(T);
+  const int stride = (2 * half_bytes + 127) / 128 * 128;
+  unsigned char* ring = smem;
+  const int appliers = blockDim.x - 32 * (1 + reducers * kWideTeam);
+  const int64_t cid = blockIdx.x / 2, ncl = gridDim.x / 2;
+  Rows rw;
+  rw.r0 = cid * rows / ncl;
+  rw.n = (int)((cid + 1) * rows / ncl - rw.r0);
+  const int n = rw.n;
+  init_pipe(pipe, stages, appliers / 32);
+  if (threadIdx.x < 6) mbar_init(&xbar[threadIdx.x / 2][threadIdx.x % 2], 2);
+  fence_mbar_init();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised
+  pdl_trigger();
+  pdl_wait();
+  volatile int* abort = &pipe.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = half / E;                 // vectors of this CTA's columns
+  const int doff = half_bytes / 16;
+  const int64_t col0 = (int64_t)rank * half; // first column of this CTA
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const void* const src[2] = {x + col0, dy + col0};
+      produce_pitched<2>(pipe, ring, stride, stages, src, rw, (size_t)hidden * sizeof(T),
+                         (uint32_t)half_bytes, abort);
+    }
+  } else if (warp <= reducers * kWideTeam) {
+    const int d = (warp - 1) / kWideTeam, tw = (warp - 1) % kWideTeam;
+    const int nthr = 32 * kWideTeam;
+    int tpar = 0, par = 0;
+    uint32_t xph0 = 0, xph1 = 0;
+    bool prev_ok = true;  // the team's last exchange (its first warp)
+    RingPos pos{0, 0u};
+    pos.advance(d, stages);
+    for (int i = d; i < n; i += reducers) {
+      const float rs = __ldg(rstd + rw.row(i));
+      const bool ok = __all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort)) &&
+                      prev_ok;
+      uint32_t all_ok;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\t"
+          "setp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.and.pred q, %2, %3, p;\n\t"
+          "selp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(all_ok)
+          : "r"((uint32_t)ok), "r"(2 + d), "r"(nthr)
+          : "memory");
+      if (!all_ok) break;
+      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+      float part[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) part[e] = 0.f;
+      for (int v = tw * 32 + lane; v < nvec; v += nthr) {
+        float xf[E], df[E], gf[E];
+        unpack<T>(st[v], xf);
+        unpack<T>(st[doff + v], df);
+        unpack<T>(ld_shared_ro(gamma + col0 + (int64_t)v * E), gf);
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[e] = fmaf(df[e] * (gf[e] + off), xf[e], part[e]);
+      }
+      const float wdot = warp_sum(pairwise<E>(part));
+      float* slot = tred[d][tpar];
+      tpar ^= 1;
+      if (lane == 0) slot[tw] = wdot;
+      asm volatile("bar.sync %0, %1;" ::"r"(2 + d), "r"(nthr) : "memory");
+      if (tw == 0) {
+        float half_dot = 0.f;
+        for (int w = 0; w < kWideTeam; ++w) half_dot += slot[w];
+        // send this CTA's half to both CTAs of the pair (itself included)
+        if (lane < 2) {
+          st_peer(&xch[d][par][rank], (uint32_t)lane, half_dot);
+          mbar_arrive_peer(&xbar[d][par], (uint32_t)lane);
+        }
+        prev_ok = __all_sync(0xffffffffu,
+                             wait_cluster_counted(&xbar[d][par], par ? xph1 : xph0, abort,
+                                                  &g_wait_timeouts));
+        if (prev_ok) {
+          if (par) xph1 ^= 1u; else xph0 ^= 1u;
+          const float dot = (xch[d][par][0] + xch[d][par][1]) * rs;
+          par ^= 1;
+          if (lane == 0) {
+            pipe.stat[pos.stage] = dot / (float)hidden;
+            mbar_arrive(&pipe.red[pos.stage]);
+            mbar_arrive(&pipe.empty[pos.stage]);
+          }
+        }
+      }
+      pos.advance(reducers, stages);
+    }
+  } else {
+    const int a = threadIdx.x - 32 * (1 + reducers * kWideTeam);
+    uint4 gp[VPT];
+    float acc[VPT][E];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = a + j * appliers;
+      gp[j] = v < nvec ? ld_shared_ro(gamma + col0 + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[j][e] = 0.f;
+    }
+    RingPos pos{0, 0u};
+    float rs_next = n > 0 ? __ldg(rstd + rw.row(0)) : 0.f;
+    bool ok = true;
+    for (int i = 0; i < n && ok; ++i) {
+      const float rs = rs_next;
+      if (i + 1 < n) rs_next = __ldg(rstd + rw.row(i + 1));
+      ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
+      ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const float c = pipe.stat[pos.stage];
+      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+      T* dxr = dx + rw.row(i) * hidden + col0;
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) opaque(gp[j]);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = a + j * appliers;
+        if (v < nvec) {
+          float xf[E], df[E], gf[E], o[E];
+          unpack<T>(st[v], xf);
+          unpack<T>(st[doff + v], df);
+          unpack<T>(gp[j], gf);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float xh = xf[e] * rs;
+            acc[j][e] = fmaf(df[e], xh, acc[j][e]);
+            o[e] = fmaf(-xh, c, df[e] * (gf[e] + off)) * rs;
+          }
+          st_vec(dxr + (int64_t)v * E, pack<T>(o));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
+      pos.advance(1, stages);
+    }
+    if (ok) {
+      float* pr = partial + cid * hidden + col0;
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = a + j * appliers;
+        if (v < nvec) {
+#pragma unroll
+          for (int e = 0; e < E; e += 4)
+            *reinterpret_cast<float4*>(pr + (int64_t)v * E + e) =
+                make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync();  // no peer stores into this CTA after it exits
+}
+
+// The paired backward: pairs of CTAs, each three 64 KB stages of half rows;
+// false when the half rows do not fit that shape.
+template <typename T>
+bool try_bwd_pair_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+  constexpr int E = Traits<T>::kVec;
+  if (a.hidden % (2 * E)) return false;
+  const int half_bytes = a.hidden / 2 * (int)sizeof(T);
+  const int stride = (2 * half_bytes + 127) / 128 * 128;
+  const int stages = kRingBudget / stride >= 3 ? 3 : 0, reducers = 3;
+  if (stages < 3) return false;
+  int appliers = 0;
+  if (pick_vpt(a.hidden / 2 / E, kWideThreads - 32 * (1 + reducers * kWideTeam), 4,
+               &appliers) != 4)
+    return false;
+  const int threads = 32 * (1 + reducers * kWideTeam) + appliers;
+  auto kern = bwd_tma_pair<T>;
+  if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return true;
+  // as many pairs as can be resident at once (one CTA per SM)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)stages * stride;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int active = 0;
+  if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) {
+    cudaGetLastError();
+    return false;
+  }
+  int64_t pairs = active;
+  if (pairs > a.rows) pairs = a.rows;
+  if (pairs > a.max_partials) pairs = a.max_partials;
+  *nparts = (int)pairs;
+  *err = launch_kernel(kern, dim3((unsigned)(2 * pairs)), dim3(threads), (size_t)stages * stride,
+                       s, 2, static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
+                       static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
+                       a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers);
+  return true;
+}
+
 // The wide-row backward: three stages without a shared gain copy and four
 // vectors per applier within kWideThreads threads; false when that does not
 // fit either.
@@ -1018,7 +1257,7 @@ bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* npar
   const int vpt = stages < 3 ? 0
                              : pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 2,
                                         &appliers);
-  if (vpt == 0) return try_bwd_wide_t<T>(a, s, err, nparts);
+  if (vpt == 0) return try_bwd_wide_t<T>(a, s, err, nparts) || try_bwd_pair_t<T>(a, s, err, nparts);
   const int grid = grid_for(a.rows, a.max_partials, err);
   if (*err != cudaSuccess) return true;
   *nparts = grid;

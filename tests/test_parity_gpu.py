@@ -105,6 +105,10 @@ SHAPES = [
     # the staged backward for 2048-vector rows (gains read through L1, four
     # vectors per applier): ragged row counts over the 152-CTA grid
     (1000, 16384, "f16"), (157, 16384, "bf16"), (301, 8192, "f32"),
+    # the paired-CTA backward for 4096-vector rows (each CTA of a cluster of
+    # two stages half of every row): ragged row counts over the pairs, fewer
+    # rows than pairs, and a width between 2048 and 4096 vectors
+    (300, 32768, "f16"), (157, 16384, "f32"), (5, 32768, "bf16"), (77, 24576, "bf16"),
 ]
 
 
