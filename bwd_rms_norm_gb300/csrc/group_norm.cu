@@ -432,38 +432,9 @@ __device__ void gn_drain(uint64_t* bar, uint32_t parity) {
   drain_phase_counted(bar, parity, &g_gn_wait_timeouts);
 }
 
-// Bounded wait on an mbarrier that peer CTAs arrive on, with acquire at
-// cluster scope: their stores made before the arrive are visible after it.
+// Cluster-scope waits, counted in this file's timeout counter.
 __device__ bool gn_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const unsigned long long t0 = global_ns();
-  for (;;) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if (*abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      atomicAdd(&g_gn_wait_timeouts, 1u);
-      return false;
-    }
-  }
-}
-
-// Arrive on the mbarrier at `local_bar`'s address in CTA `peer`, releasing
-// this thread's earlier stores at cluster scope.
-__device__ __forceinline__ void arrive_peer(uint64_t* local_bar, uint32_t peer) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(smem_u32(local_bar)), "r"(peer));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
-               : "memory");
+  return wait_cluster_counted(bar, parity, abort, &g_gn_wait_timeouts);
 }
 
 // Named barrier 1 over the nthreads appliers; true when `ok` holds in every
@@ -539,7 +510,7 @@ __device__ __forceinline__ bool exchange(GnPipe& pp, int d, int par, uint32_t xp
                                          volatile int* abort) {
   if (lane < csize) {
     st_peer2(&pp.xch[d][par][rank], (uint32_t)lane, mine);
-    arrive_peer(&pp.xbar[d][par], (uint32_t)lane);
+    mbar_arrive_peer(&pp.xbar[d][par], (uint32_t)lane);
   }
   return __all_sync(kFull, gn_wait_cluster(&pp.xbar[d][par], xph, abort));
 }

@@ -20,22 +20,52 @@
 namespace rmsn {
 namespace {
 
+// Maximum of packed pairs of a 16-bit type (exact: no rounding involved;
+// a NaN loses to a number, as with fmaxf).
+__device__ __forceinline__ uint32_t max_pair(uint32_t a, uint32_t b, __nv_bfloat16) {
+  __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a),
+                             *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t max_pair(uint32_t a, uint32_t b, __half) {
+  __half2 r = __hmax2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 // The thread's max over the in-range elements of its VPT packed vectors.
+// 16-bit types compare packed pairs and widen only the final pair.
 template <typename T, int VPT>
 __device__ __forceinline__ float local_max(const uint4 (&xv)[VPT], int first, int stride,
                                            int nvec) {
   constexpr int E = Traits<T>::kVec;
-  float m = -INFINITY;
+  if constexpr (sizeof(T) == 2) {
+    uint32_t m2 = 0;
+    bool any = false;
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    if (first + k * stride < nvec) {
-      float f[E];
-      unpack<T>(xv[k], f);
-#pragma unroll
-      for (int e = 0; e < E; ++e) m = fmaxf(m, f[e]);
+    for (int k = 0; k < VPT; ++k) {
+      if (first + k * stride < nvec) {
+        const uint32_t w = max_pair(max_pair(xv[k].x, xv[k].y, T()),
+                                    max_pair(xv[k].z, xv[k].w, T()), T());
+        m2 = any ? max_pair(m2, w, T()) : w;
+        any = true;
+      }
     }
+    if (!any) return -INFINITY;
+    const T* h = reinterpret_cast<const T*>(&m2);
+    return fmaxf(Traits<T>::to_f(h[0]), Traits<T>::to_f(h[1]));
+  } else {
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      if (first + k * stride < nvec) {
+        float f[E];
+        unpack<T>(xv[k], f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) m = fmaxf(m, f[e]);
+      }
+    }
+    return m;
   }
-  return m;
 }
 
 // One warp per row (8 rows per 256-thread CTA); exp(x - m) kept in fp32

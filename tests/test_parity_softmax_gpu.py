@@ -94,12 +94,14 @@ def test_softmax_unaligned(L, dtype):
     run_and_check(L, w, to_dev=_misaligned_copy)
 
 
-def test_softmax_large_logits_and_masking(L):
+@pytest.mark.parametrize("cols", [512, 4096])
+def test_softmax_large_logits_and_masking(L, cols):
     """Logits near 1e4 (exp overflows without the max shift), rows with -inf
     entries (masked positions give exactly 0), and a fully masked row (NaN,
-    as the formula gives)."""
+    as the formula gives); rows for one warp (512) and one CTA (4096), whose
+    16-bit maxima are taken on packed pairs."""
     g = torch.Generator().manual_seed(11)
-    x = torch.randn(6, 512, generator=g) * 3.0
+    x = torch.randn(6, cols, generator=g) * 3.0
     x[0] += 1.0e4
     x[1, ::3] = float("-inf")
     x[2, 100:] = float("-inf")
@@ -110,8 +112,11 @@ def test_softmax_large_logits_and_masking(L):
     check_forward(L, x, "f32", np.array(ok))
     assert torch.all(y[1, ::3] == 0) and torch.all(y[2, 100:] == 0)
     assert torch.all(torch.isnan(y[3]))
-    xb = x.to(torch.bfloat16)
-    check_forward(L, xb, "bf16", np.array(ok))
+    for dt, fmt in ((torch.bfloat16, "bf16"), (torch.float16, "f16")):
+        xh = x.to(dt)
+        check_forward(L, xh, fmt, np.array(ok))
+        yh = L.softmax_fwd(xh.cuda()).cpu()
+        assert torch.all(yh[1, ::3] == 0) and torch.all(torch.isnan(yh[3]))
 
 
 def test_softmax_rows_sum_to_one(L):
