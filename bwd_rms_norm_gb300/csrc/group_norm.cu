@@ -12,15 +12,17 @@
 // dW = sum dy * x_hat and dB = sum dy over samples and positions.
 //
 // A group is long (65536 to 262144 elements in the shapes the PR times), so
-// it is split over a thread-block cluster of up to 16 CTAs, each holding its
-// slice in registers; the group sums go through distributed shared memory
-// (cluster.cuh), and every element is read once.  The backward's per-channel
-// sums are reduced inside the CTA in a fixed order (per-vector sums in
-// shared memory, one warp per channel) and written as fp32 partial rows
-// [n * csize, 2C] (dW columns, then dB), which the column-sum kernel of
-// bwd.cu reduces in a fixed order: the result is deterministic.  Groups
-// that are not 16-byte aligned, or too long for 16 CTAs, run scalar kernels
-// (one CTA per group).
+// it is split over a thread-block cluster of up to 16 CTAs whose group sums
+// go through distributed shared memory (cluster.cuh).  The forward holds a
+// CTA's slice in registers (gn_fwd_cluster) or streams it through a
+// shared-memory ring (gn_fwd_pipe), reading every element once.  The
+// backward (gn_bwd_l2) reads x and dy twice: from HBM through a ring for
+// its sums, then from L2 for dx.  Its per-channel sums are reduced inside
+// the CTA in a fixed order (per-vector sums in shared memory, warps per
+// channel) and written as fp32 partial rows [n * csize, 2C] (dW columns,
+// then dB), which the column-sum kernel of bwd.cu reduces in a fixed order:
+// the result is deterministic.  Groups that are not 16-byte aligned, or too
+// long for these kernels, run scalar kernels (one CTA per group).
 #include <mutex>
 
 #include "cluster.cuh"
@@ -29,9 +31,9 @@
 namespace rmsn {
 namespace {
 
-// Most 16-byte vectors one CTA holds: 8 a thread at 512 threads (x, and in
-// the backward dy as well: 64 of the 128 registers a thread).  Cluster CTAs
-// stay at 512 threads so that 16 of them fit one GPC.
+// Most 16-byte vectors one CTA of the register forward holds: 8 a thread at
+// 512 threads.  Cluster CTAs stay at 512 threads so that 16 of them fit one
+// GPC.
 constexpr int kGnMaxVec = 4096;
 constexpr int kGnThreads = 512;
 
@@ -106,151 +108,6 @@ __global__ void __launch_bounds__(kGnThreads) gn_fwd_cluster(
   }
 }
 
-template <typename T, int VPT>
-__global__ void __launch_bounds__(kGnThreads) gn_bwd_cluster(
-    const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
-    const float* __restrict__ mean, const float* __restrict__ rstd, T* __restrict__ dx,
-    float* __restrict__ partial, int M, int spv, int Cg, int G, int C, int csize) {
-  constexpr int E = Traits<T>::kVec;
-  __shared__ float2 vsum[kGnMaxVec];
-  __shared__ float2 red[64];
-  __shared__ float2 slots[2 * kMaxCluster];
-  const uint32_t rank = csize > 1 ? cta_rank() : 0u;
-  const int64_t grp = blockIdx.x / csize;
-  const int64_t n = grp / G;
-  const int cbase = (int)(grp % G) * Cg;
-  const int nv = M / E / csize;
-  const int base = (int)rank * nv;
-  const T* xg = x + grp * M;
-  const T* dg = dy + grp * M;
-  if (csize > 1) cluster_sync();
-  pdl_trigger();
-  pdl_wait();
-  const float mu = __ldg(mean + grp), rs = __ldg(rstd + grp);
-  uint4 xv[VPT], dv[VPT];
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = threadIdx.x + k * blockDim.x;
-    const bool in = v < nv;
-    xv[k] = in ? ld_stream(xg + (int64_t)(base + v) * E) : make_uint4(0, 0, 0, 0);
-    dv[k] = in ? ld_stream(dg + (int64_t)(base + v) * E) : make_uint4(0, 0, 0, 0);
-  }
-  float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = threadIdx.x + k * blockDim.x;
-    if (v < nv) {
-      const float w = Traits<T>::to_f(gamma[cbase + (base + v) / spv]);
-      float xf[E], df[E];
-      unpack<T>(xv[k], xf);
-      unpack<T>(dv[k], df);
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float gd = df[e] * w;
-        s1 += gd;
-        s2 = fmaf(gd, xf[e] - mu, s2);
-      }
-    }
-  }
-  const float2 t = csize > 1 ? cluster_sum2(s1, s2, red, slots, 0, rank, csize)
-                             : block_sum2(s1, s2, red, 0);
-  const float c1 = t.x / (float)M, c2 = t.y * rs / (float)M;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    // unpack again below rather than hold both rows unpacked across the sum
-    opaque(xv[k]);
-    opaque(dv[k]);
-  }
-  T* xo = dx + grp * M;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = threadIdx.x + k * blockDim.x;
-    if (v < nv) {
-      const float w = Traits<T>::to_f(gamma[cbase + (base + v) / spv]);
-      float xf[E], df[E], o[E];
-      unpack<T>(xv[k], xf);
-      unpack<T>(dv[k], df);
-      float pg = 0.f, pb = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float xh = (xf[e] - mu) * rs;
-        o[e] = fmaf(-xh, c2, df[e] * w - c1) * rs;
-        pg = fmaf(df[e], xh, pg);
-        pb += df[e];
-      }
-      st_vec(xo + (int64_t)(base + v) * E, pack<T>(o));
-      vsum[v] = make_float2(pg, pb);
-    }
-  }
-  __syncthreads();
-  // Per-channel sums over this slice, in a fixed order.  The slice touches
-  // channels c_lo..c_hi of the group.  With at least as many channels as
-  // warps, warp w sums channels c_lo + w, c_lo + w + nwarps, ... (lanes
-  // striding over the channel's vectors, then a butterfly).  With fewer,
-  // each channel's vectors are split into wpc equal runs, one warp each,
-  // whose two sums meet in shared memory and are added in run order.
-  // Channels of the group this slice does not touch get 0, so that every
-  // column of the partial row is written.
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-  float* prow = partial + (n * csize + rank) * (int64_t)(2 * C);
-  const int c_lo = base / spv, c_hi = (base + nv - 1) / spv;
-  const int nch = c_hi - c_lo + 1;
-  for (int cl = threadIdx.x; cl < Cg; cl += blockDim.x) {
-    if (cl < c_lo || cl > c_hi) {
-      prow[cbase + cl] = 0.f;
-      prow[C + cbase + cl] = 0.f;
-    }
-  }
-  auto run_sum = [&](int v0, int v1) {
-    float a = 0.f, b = 0.f;
-    for (int v = v0 + lane; v < v1; v += 32) {
-      a += vsum[v].x;
-      b += vsum[v].y;
-    }
-    return make_float2(warp_sum(a), warp_sum(b));
-  };
-  auto range_of = [&](int cl, int* v0, int* v1) {
-    *v0 = cl * spv - base;
-    *v1 = (cl + 1) * spv - base;
-    if (*v0 < 0) *v0 = 0;
-    if (*v1 > nv) *v1 = nv;
-  };
-  if (nch >= nwarps) {
-    for (int cl = c_lo + warp; cl <= c_hi; cl += nwarps) {
-      int v0, v1;
-      range_of(cl, &v0, &v1);
-      const float2 t2 = run_sum(v0, v1);
-      if (lane == 0) {
-        prow[cbase + cl] = t2.x;
-        prow[C + cbase + cl] = t2.y;
-      }
-    }
-  } else {
-    const int wpc = nwarps / nch;  // warps per channel
-    __shared__ float2 wsum[32];
-    if (warp < nch * wpc) {
-      const int cl = c_lo + warp / wpc, part = warp % wpc;
-      int v0, v1;
-      range_of(cl, &v0, &v1);
-      const int len = v1 - v0;
-      const int a0 = v0 + (int)((int64_t)len * part / wpc);
-      const int a1 = v0 + (int)((int64_t)len * (part + 1) / wpc);
-      const float2 t2 = run_sum(a0, a1);
-      if (lane == 0) wsum[warp] = t2;
-    }
-    __syncthreads();
-    if (threadIdx.x < nch) {
-      float a = 0.f, b = 0.f;
-      for (int q = 0; q < wpc; ++q) {
-        a += wsum[threadIdx.x * wpc + q].x;
-        b += wsum[threadIdx.x * wpc + q].y;
-      }
-      prow[cbase + c_lo + threadIdx.x] = a;
-      prow[C + cbase + c_lo + threadIdx.x] = b;
-    }
-  }
-}
 
 // One CTA per group, any alignment: scalar loads, the group read from L2 in
 // every pass.
@@ -337,7 +194,7 @@ __global__ void __launch_bounds__(256) gn_bwd_scalar(
 }
 
 // ---------------------------------------------------------------------------
-// Persistent, TMA-fed, warp-specialised pipeline.  One cluster of csize
+// Persistent, TMA-fed, warp-specialised forward.  One cluster of csize
 // CTAs (one CTA per SM) walks a contiguous range of groups; CTA rank q owns
 // slice q of every group (nv 16-byte vectors).  Three roles meet at
 // per-stage mbarriers, as in the RMSNorm staged kernels:
@@ -354,9 +211,9 @@ __global__ void __launch_bounds__(256) gn_bwd_scalar(
 //   appliers (the other warps)  walk every group in order and write the
 //       outputs of their vectors of the slice.
 //
-// The forward exchanges (slice mean, slice centred sum of squares) and
-// combines them in rank order (Chan's formula for slices of equal length);
-// the backward exchanges (sum g, sum g * (x - mean)).  A reducer waits for
+// A reducer exchanges (slice mean, slice centred sum of squares) and
+// combines them in rank order (Chan's formula for slices of equal length).
+// It waits for
 // its peers while the appliers work on earlier groups and the producer's
 // copies of later groups are in flight.  The stage count is a multiple of
 // the reducer count, so that every mbarrier waiter sees every phase of the
@@ -367,10 +224,9 @@ __global__ void __launch_bounds__(256) gn_bwd_scalar(
 // every group with one group of lookahead: this split is 25-35% faster.
 //
 // Every wait is bounded (about one second); a wait that runs out counts in
-// g_gn_wait_timeouts and aborts the CTA; decisions are taken per warp (and,
-// among the appliers of the backward, which share a named barrier, with a
-// predicate-reducing barrier), and every CTA ends with a cluster barrier,
-// so that no CTA exits while a peer may still store into its shared memory.
+// g_gn_wait_timeouts and aborts the CTA; decisions are taken per warp, and
+// every CTA ends with a cluster barrier, so that no CTA exits while a peer
+// may still store into its shared memory.
 // ---------------------------------------------------------------------------
 __device__ unsigned int g_gn_wait_timeouts;
 
@@ -385,11 +241,10 @@ struct GnPipe {
   uint64_t full[kGnStages];    // the stage's bulk copies landed
   uint64_t red[kGnStages];     // the stage's group statistics are in stat[]
   uint64_t empty[kGnStages];   // its reducer and every applier warp are done
-  float2 stat[kGnStages];      // forward (mean, rstd); backward (c1, c2)
+  float2 stat[kGnStages];      // the group's (mean, rstd)
   uint64_t xbar[kGnReducers][2];            // a reducer's pairs arrived
   float2 xch[kGnReducers][2][kMaxCluster];  // ... by sender rank
   float2 tred[kGnReducers][2][kGnTeamMax];  // team-warp partial sums
-  float2 wsum[32];             // applier-warp channel sums (backward)
   int abort;
 };
 
@@ -435,25 +290,6 @@ __device__ void gn_drain(uint64_t* bar, uint32_t parity) {
 // Cluster-scope waits, counted in this file's timeout counter.
 __device__ bool gn_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
   return wait_cluster_counted(bar, parity, abort, &g_gn_wait_timeouts);
-}
-
-// Named barrier 1 over the nthreads appliers; true when `ok` holds in every
-// one of them.
-__device__ __forceinline__ bool appliers_all(bool ok, int nthreads) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)ok), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ void appliers_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ void gn_pipe_init(GnPipe& pp, int stages, int applier_warps,
@@ -684,148 +520,225 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_fwd_pipe(
   if (csize > 1) cluster_sync();  // no peer stores into this CTA after it exits
 }
 
+
+// ---------------------------------------------------------------------------
+// Backward with the group held in L2 rather than in shared memory.  A
+// cluster of csize CTAs (one CTA per SM) walks a contiguous range of groups;
+// CTA rank q owns slice q of every group (nv 16-byte vectors).  Roles:
+//
+//   producer (warp 0, one thread)  streams the slices, in chunks of
+//       kL2Chunk vectors of x and of dy, into a ring of shared-memory
+//       stages with 1D bulk copies                              -> full[s]
+//   reducers (warps 1 .. kL2Red)  take every chunk: per thread the sums of
+//       W[c] * dy and W[c] * dy * (x - mean), per vector (dy * (x - mean),
+//       dy) into shared memory; at the end of the slice they reduce the
+//       per-vector sums per channel into the partial row, and thread 0
+//       posts the CTA's pair (warps in a fixed order)          -> sum_ready
+//   exchanger (the next warp)  trades the pair with the cluster through
+//       distributed shared memory, adds the csize pairs in rank order and
+//       posts (c1, c2)                                          -> red
+//   appliers (the other warps)  read the slice again, from L2 where the
+//       producer's copies left it, and write dx                 -> free
+//
+// The ring only has to cover the latency of HBM, not a whole slice, so the
+// cluster size is free of shared memory: the host picks it so that two
+// groups of slices of every resident CTA fit in a fraction of L2 (the
+// reducers start group i + 2 only after the appliers have finished group
+// i).  Per-group buffers and mbarriers alternate with b = i & 1; the phase
+// of group i on them is (i >> 1) & 1.  Every wait is bounded, the reducers
+// take their decisions at predicate-reducing barriers, and every CTA of a
+// cluster ends at a cluster barrier.
+// ---------------------------------------------------------------------------
+constexpr int kL2Threads = 768;
+constexpr int kL2Red = 8;                                  // reducer warps
+constexpr int kL2App = kL2Threads / 32 - kL2Red - 2;       // applier warps
+constexpr int kL2Chunk = 512;                              // vectors of x (and dy) a stage
+constexpr int kL2Stages = 4;
+constexpr int kL2Unroll = 4;                               // vectors an applier loads at once
+constexpr int kL2MaxVec = 8192;                            // slice vectors
+static_assert(kL2Chunk % (32 * kL2Red) == 0, "every reducer thread takes whole chunks");
+
+struct GnL2 {
+  uint64_t full[kL2Stages], empty[kL2Stages];
+  uint64_t sum_ready[2], red[2], free[2], xbar[2];
+  float2 csum[2];                 // the CTA's pair of group i
+  float2 stat[2];                 // (c1, c2) of group i
+  float2 wred[kL2Red];            // reducer-warp pairs
+  float2 xch[2][kMaxCluster];     // peers' pairs by sender rank
+  float2 wsum[kL2Red];            // channel part sums
+  int abort;
+};
+
+// Reducer barrier (named barrier 2 over the reducer warps); the voting form
+// tells whether `ok` held in every reducer thread.
+__device__ __forceinline__ bool red_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 2, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(32 * kL2Red)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void red_sync() {
+  asm volatile("bar.sync 2, %0;" ::"r"(32 * kL2Red) : "memory");
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
+__global__ void __launch_bounds__(kL2Threads, 1) gn_bwd_l2(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ mean, const float* __restrict__ rstd, T* __restrict__ dx,
     float* __restrict__ partial, int64_t ngroups, int M, int spv, int Cg, int G, int C,
-    int csize, int stages, int nv, int ntw) {
+    int csize, int nv, int stages) {
   constexpr int E = Traits<T>::kVec;
-  extern __shared__ __align__(128) unsigned char ring[];
-  __shared__ GnPipe pp;
+  constexpr int CH = kL2Chunk;
+  constexpr uint32_t stride = 2u * CH * 16u;
+  extern __shared__ __align__(128) unsigned char ring[];   // stages x stride, then vsum
+  float2* vsum = reinterpret_cast<float2*>(ring + (size_t)stages * stride);
+  __shared__ GnL2 st;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int napp = blockDim.x - 32 * (1 + kGnReducers * ntw);
   const uint32_t rank = csize > 1 ? cta_rank() : 0u;
   const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
   const int64_t g0 = cid * ngroups / ncl;
   const int count = (int)((cid + 1) * ngroups / ncl - g0);
-  const uint32_t sb = (uint32_t)nv * 16u;
-  float2* vsum = reinterpret_cast<float2*>(ring + (size_t)stages * 2 * sb);
-  gn_pipe_init(pp, stages, napp / 32, csize);
+  const int vbase = (int)rank * nv;
+  if (threadIdx.x == 0) st.abort = 0;
+  if (threadIdx.x < stages) {
+    mbar_init(&st.full[threadIdx.x], 1);
+    mbar_init(&st.empty[threadIdx.x], kL2Red);
+  }
+  if (threadIdx.x < 2) {
+    mbar_init(&st.sum_ready[threadIdx.x], 1);
+    mbar_init(&st.red[threadIdx.x], 1);
+    mbar_init(&st.free[threadIdx.x], kL2App);
+    mbar_init(&st.xbar[threadIdx.x], csize);
+  }
+  fence_mbar_init();
   __syncthreads();
   if (csize > 1) cluster_sync();
   pdl_trigger();
   pdl_wait();
-  volatile int* abort = &pp.abort;
-  const int vbase = (int)rank * nv;
+  volatile int* abort = &st.abort;
+
   if (warp == 0) {
     if (lane == 0) {
-      const unsigned char* const src[2] = {reinterpret_cast<const unsigned char*>(x),
-                                           reinterpret_cast<const unsigned char*>(dy)};
-      gn_produce<2>(pp, ring, stages, sb, src, g0, count, (int64_t)M * sizeof(T),
-                    (int64_t)vbase * 16, abort);
-    }
-  } else if (warp <= kGnReducers * ntw) {
-    const int d = (warp - 1) / ntw, tw = (warp - 1) % ntw;
-    const int first = tw * 32 + lane, step = 32 * ntw;
-    int stage = d, par = 0, tpar = 0;
-    uint32_t ph = 0, xph0 = 0, xph1 = 0;
-    bool prev_ok = true;
-    for (int i = d; i < count; i += kGnReducers) {
-      const int64_t grp = g0 + i;
-      const float mu = __ldg(mean + grp), rs = __ldg(rstd + grp);
-      const int cbase = (int)(grp % G) * Cg;
-      const bool ok = __all_sync(kFull, gn_wait(&pp.full[stage], ph, abort)) && prev_ok;
-      if (!team_all(ok, d, 32 * ntw)) break;
-      const uint4* sx = reinterpret_cast<const uint4*>(ring + (size_t)stage * 2 * sb);
-      const uint4* sd = sx + nv;
-      float p1[E], p2[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) p1[e] = p2[e] = 0.f;
-      ChanWalk cw(vbase + first, step, spv);
-#pragma unroll 2
-      for (int v = first; v < nv; v += step, cw.next()) {
-        const float w = Traits<T>::to_f(gamma[cbase + cw.q]);
-        float xf[E], df[E];
-        unpack<T>(sx[v], xf);
-        unpack<T>(sd[v], df);
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float gd = df[e] * w;
-          p1[e] += gd;
-          p2[e] = fmaf(gd, xf[e] - mu, p2[e]);
-        }
-      }
-      float2 t = team_sum2(pp, make_float2(lane_total<E>(p1), lane_total<E>(p2)), d, tw, ntw,
-                           tpar, lane);
-      if (tw == 0) {
-        if (csize > 1) {
-          prev_ok = exchange(pp, d, par, par ? xph1 : xph0, t, rank, csize, lane, abort);
-          if (prev_ok) {
-            if (par) xph1 ^= 1u; else xph0 ^= 1u;
-            t = make_float2(0.f, 0.f);
-            for (int r = 0; r < csize; ++r) {
-              t.x += pp.xch[d][par][r].x;
-              t.y += pp.xch[d][par][r].y;
-            }
-            par ^= 1;
+      int stage = 0;
+      uint32_t ph = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int i = 0; i < count && ok; ++i) {
+        const int64_t off = ((g0 + i) * M + (int64_t)vbase * E) * (int64_t)sizeof(T);
+        const unsigned char* xs = reinterpret_cast<const unsigned char*>(x) + off;
+        const unsigned char* ds = reinterpret_cast<const unsigned char*>(dy) + off;
+        for (int c0 = 0; c0 < nv; c0 += CH) {
+          if (issued >= stages && !gn_wait(&st.empty[stage], ph ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bytes = (uint32_t)(nv - c0 < CH ? nv - c0 : CH) * 16u;
+          unsigned char* dst = ring + (size_t)stage * stride;
+          mbar_arrive_expect_tx(&st.full[stage], 2u * bytes);
+          bulk_load(dst, xs + (size_t)c0 * 16, bytes, &st.full[stage]);
+          bulk_load(dst + CH * 16, ds + (size_t)c0 * 16, bytes, &st.full[stage]);
+          ++issued;
+          if (++stage == stages) {
+            stage = 0;
+            ph ^= 1u;
           }
         }
-        if (prev_ok && lane == 0) {
-          pp.stat[stage] = make_float2(t.x / (float)M, t.y * rs / (float)M);
-          mbar_arrive(&pp.red[stage]);
-          mbar_arrive(&pp.empty[stage]);
-        }
       }
-      stage += kGnReducers;
-      if (stage >= stages) {
-        stage -= stages;
-        ph ^= 1u;
+      // every copy issued must land before the CTA may exit: the latest
+      // min(issued, stages) issues are the last use of each stage
+      const int outstanding = issued < stages ? (int)issued : stages;
+      for (int q = 0; q < outstanding; ++q) {
+        if (stage == 0) {
+          stage = stages - 1;
+          ph ^= 1u;
+        } else {
+          --stage;
+        }
+        gn_drain(&st.full[stage], ph);
       }
     }
-  } else {
-    const int a = threadIdx.x - 32 * (1 + kGnReducers * ntw);
-    const int cwi = a >> 5, ncw = napp >> 5;
+  } else if (warp <= kL2Red) {
+    const int rw = warp - 1, rt = threadIdx.x - 32, step = 32 * kL2Red;
     const int c_lo = vbase / spv, c_hi = (vbase + nv - 1) / spv;
     const int nch = c_hi - c_lo + 1;
     int stage = 0;
     uint32_t ph = 0;
     for (int i = 0; i < count; ++i) {
+      const int b = i & 1;
       const int64_t grp = g0 + i;
-      const float mu = __ldg(mean + grp), rs = __ldg(rstd + grp);
+      bool ok = true;
+      if (i >= 2) ok = gn_wait(&st.free[b], ((i - 2) >> 1) & 1, abort);
+      if (!red_all(__all_sync(kFull, ok))) break;
+      const float mu = __ldg(mean + grp);
       const int cbase = (int)(grp % G) * Cg;
-      bool ok = gn_wait(&pp.red[stage], ph, abort);
-      ok = ok && gn_wait(&pp.full[stage], ph, abort);
-      if (!appliers_all(ok, napp)) break;
-      const float2 cc = pp.stat[stage];
-      const uint4* sx = reinterpret_cast<const uint4*>(ring + (size_t)stage * 2 * sb);
-      const uint4* sd = sx + nv;
-      T* xo = dx + grp * M;
-      ChanWalk chw(vbase + a, napp, spv);
-      for (int v = a; v < nv; v += napp, chw.next()) {
-        const float w = Traits<T>::to_f(gamma[cbase + chw.q]);
-        float xf[E], df[E], o[E];
-        unpack<T>(sx[v], xf);
-        unpack<T>(sd[v], df);
-        float pg = 0.f, pb = 0.f;
+      float p1 = 0.f, p2 = 0.f;
+      ChanWalk cw(vbase + rt, step, spv);
+      for (int c0 = 0; c0 < nv && ok; c0 += CH) {
+        ok = __all_sync(kFull, gn_wait(&st.full[stage], ph, abort));
+        if (!ok) break;
+        const uint4* sx = reinterpret_cast<const uint4*>(ring + (size_t)stage * stride);
+        const uint4* sd = sx + CH;
+        const int len = nv - c0 < CH ? nv - c0 : CH;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float xh = (xf[e] - mu) * rs;
-          o[e] = fmaf(-xh, cc.y, df[e] * w - cc.x) * rs;
-          pg = fmaf(df[e], xh, pg);
-          pb += df[e];
+        for (int k = 0; k < CH / (32 * kL2Red); ++k) {
+          const int l = rt + k * step;
+          if (l < len) {
+            float xf[E], df[E];
+            unpack<T>(sx[l], xf);
+            unpack<T>(sd[l], df);
+            float q2 = 0.f, sb = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              q2 = fmaf(df[e], xf[e] - mu, q2);
+              sb += df[e];
+            }
+            const float w = Traits<T>::to_f(gamma[cbase + cw.q]);
+            p1 = fmaf(w, sb, p1);
+            p2 = fmaf(w, q2, p2);
+            vsum[c0 + l] = make_float2(q2, sb);
+          }
+          cw.next();
         }
-        st_vec(xo + (int64_t)(vbase + v) * E, pack<T>(o));
-        vsum[v] = make_float2(pg, pb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&st.empty[stage]);
+        if (++stage == stages) {
+          stage = 0;
+          ph ^= 1u;
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pp.empty[stage]);  // the stage is no longer read
-      if (++stage == stages) {
-        stage = 0;
-        ph ^= 1u;
+      p1 = warp_sum(p1);
+      p2 = warp_sum(p2);
+      if (lane == 0) st.wred[rw] = make_float2(p1, p2);
+      if (!red_all(ok)) break;  // vsum and wred complete
+      if (rt == 0) {
+        float2 t = make_float2(0.f, 0.f);
+        for (int w = 0; w < kL2Red; ++w) {
+          t.x += st.wred[w].x;
+          t.y += st.wred[w].y;
+        }
+        st.csum[b] = t;
+        mbar_arrive(&st.sum_ready[b]);
       }
-      appliers_sync(napp);  // vsum complete
-      // Per-channel sums of this slice in a fixed order (as in
-      // gn_bwd_cluster); channels of the group it does not touch get 0.
+      // Per-channel sums of this slice in a fixed order: dW = rstd * sum
+      // dy * (x - mean), dB = sum dy; channels of the group the slice does
+      // not touch get 0.  (The next group's first barrier orders these
+      // reads of vsum and wred before their next writes.)
+      const float rs = __ldg(rstd + grp);
       float* prow = partial + ((grp / G) * csize + rank) * (int64_t)(2 * C);
-      for (int cl = a; cl < Cg; cl += napp) {
+      for (int cl = rt; cl < Cg; cl += step) {
         if (cl < c_lo || cl > c_hi) {
           prow[cbase + cl] = 0.f;
           prow[C + cbase + cl] = 0.f;
         }
       }
-      if (nch >= ncw) {
-        for (int cl = c_lo + cwi; cl <= c_hi; cl += ncw) {
+      if (nch >= kL2Red) {
+        for (int cl = c_lo + rw; cl <= c_hi; cl += kL2Red) {
           int v0 = cl * spv - vbase, v1 = (cl + 1) * spv - vbase;
           if (v0 < 0) v0 = 0;
           if (v1 > nv) v1 = nv;
@@ -837,14 +750,14 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
           s1 = warp_sum(s1);
           s2 = warp_sum(s2);
           if (lane == 0) {
-            prow[cbase + cl] = s1;
+            prow[cbase + cl] = rs * s1;
             prow[C + cbase + cl] = s2;
           }
         }
       } else {
-        const int wpc = ncw / nch;
-        if (cwi < nch * wpc) {
-          const int cl = c_lo + cwi / wpc, part = cwi % wpc;
+        const int wpc = kL2Red / nch;
+        if (rw < nch * wpc) {
+          const int cl = c_lo + rw / wpc, part = rw % wpc;
           int v0 = cl * spv - vbase, v1 = (cl + 1) * spv - vbase;
           if (v0 < 0) v0 = 0;
           if (v1 > nv) v1 = nv;
@@ -858,20 +771,91 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
           }
           s1 = warp_sum(s1);
           s2 = warp_sum(s2);
-          if (lane == 0) pp.wsum[cwi] = make_float2(s1, s2);
+          if (lane == 0) st.wsum[rw] = make_float2(s1, s2);
         }
-        appliers_sync(napp);
-        if (a < nch) {
+        red_sync();
+        if (rt < nch) {
           float s1 = 0.f, s2 = 0.f;
           for (int q = 0; q < wpc; ++q) {
-            s1 += pp.wsum[a * wpc + q].x;
-            s2 += pp.wsum[a * wpc + q].y;
+            s1 += st.wsum[rt * wpc + q].x;
+            s2 += st.wsum[rt * wpc + q].y;
           }
-          prow[cbase + c_lo + a] = s1;
-          prow[C + cbase + c_lo + a] = s2;
+          prow[cbase + c_lo + rt] = rs * s1;
+          prow[C + cbase + c_lo + rt] = s2;
         }
       }
-      appliers_sync(napp);  // vsum and wsum are free for the next group
+    }
+  } else if (warp == kL2Red + 1) {
+    for (int i = 0; i < count; ++i) {
+      const int b = i & 1;
+      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+      const int64_t grp = g0 + i;
+      if (!__all_sync(kFull, gn_wait(&st.sum_ready[b], ph, abort))) break;
+      float2 t = st.csum[b];
+      if (csize > 1) {
+        if (lane < csize) {
+          st_peer2(&st.xch[b][rank], (uint32_t)lane, t);
+          mbar_arrive_peer(&st.xbar[b], (uint32_t)lane);
+        }
+        if (!__all_sync(kFull, gn_wait_cluster(&st.xbar[b], ph, abort))) break;
+        t = make_float2(0.f, 0.f);
+        for (int r = 0; r < csize; ++r) {
+          t.x += st.xch[b][r].x;
+          t.y += st.xch[b][r].y;
+        }
+      }
+      if (lane == 0) {
+        const float rs = __ldg(rstd + grp);
+        st.stat[b] = make_float2(t.x / (float)M, t.y * rs / (float)M);
+        mbar_arrive(&st.red[b]);
+      }
+    }
+  } else {
+    constexpr int U = kL2Unroll;
+    const int at = threadIdx.x - 32 * (kL2Red + 2), step = 32 * kL2App;
+    for (int i = 0; i < count; ++i) {
+      const int b = i & 1;
+      const int64_t grp = g0 + i;
+      if (!__all_sync(kFull, gn_wait(&st.red[b], (uint32_t)(i >> 1) & 1u, abort))) break;
+      const float2 cc = st.stat[b];
+      const float mu = __ldg(mean + grp), rs = __ldg(rstd + grp);
+      const int cbase = (int)(grp % G) * Cg;
+      const T* xs = x + grp * M + (int64_t)vbase * E;
+      const T* ds = dy + grp * M + (int64_t)vbase * E;
+      T* xo = dx + grp * M + (int64_t)vbase * E;
+      ChanWalk cw(vbase + at, step, spv);
+      for (int v0 = at; v0 < nv; v0 += U * step) {
+        uint4 xv[U], dv[U];
+        int ch[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * step;
+          ch[u] = cw.q;
+          cw.next();
+          if (v < nv) {
+            xv[u] = ld_stream(xs + (int64_t)v * E);
+            dv[u] = ld_stream(ds + (int64_t)v * E);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * step;
+          if (v < nv) {
+            const float w = Traits<T>::to_f(gamma[cbase + ch[u]]);
+            float xf[E], df[E], o[E];
+            unpack<T>(xv[u], xf);
+            unpack<T>(dv[u], df);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              const float xh = (xf[e] - mu) * rs;
+              o[e] = fmaf(-xh, cc.y, df[e] * w - cc.x) * rs;
+            }
+            st_vec(xo + (int64_t)v * E, pack<T>(o));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st.free[b]);
     }
   }
   __syncwarp();
@@ -879,9 +863,8 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_bwd_pipe(
 }
 
 // Pipeline shape: the smallest cluster (1..16 CTAs) whose slices leave at
-// least min_stages ring stages (a multiple of the reducer count) in kGnSmem
-// (the backward also keeps a float2 per slice vector); false when none
-// does.
+// least min_stages ring stages (a multiple of the reducer count) in kGnSmem;
+// false when none does.
 struct PipeShape {
   int csize, stages, nv, threads;
   size_t smem;
@@ -891,22 +874,20 @@ struct PipeShape {
 // Warps a reducer team (measured on GB300: 2 beat 1, 3 and 4).
 constexpr int kGnTeamWarps = 2;
 
-bool pick_pipe_min(int nvec, bool bwd, int min_stages, PipeShape* ps) {
+bool pick_pipe_min(int nvec, int min_stages, PipeShape* ps) {
   for (int k = 1; k <= kMaxCluster; k *= 2) {
     if (nvec % k) continue;
     const int nv = nvec / k;
     const size_t sb = (size_t)nv * 16;
-    const size_t per = bwd ? 2 * sb : sb;
-    const size_t extra = bwd ? (size_t)nv * sizeof(float2) : 0;
-    if (extra + (size_t)min_stages * per > (size_t)kGnSmem) continue;
-    int st = (int)(((size_t)kGnSmem - extra) / per);
+    if ((size_t)min_stages * sb > (size_t)kGnSmem) continue;
+    int st = (int)((size_t)kGnSmem / sb);
     if (st > kGnStages) st = kGnStages;
     st -= st % kGnReducers;
     const int ntw = kGnTeamWarps;
     int apps = (nv + 31) / 32;
     const int max_apps = kGnThreadsMax / 32 - 1 - kGnReducers * ntw;
     if (apps > max_apps) apps = max_apps;
-    *ps = PipeShape{k, st, nv, 32 * (1 + kGnReducers * ntw + apps), (size_t)st * per + extra, ntw};
+    *ps = PipeShape{k, st, nv, 32 * (1 + kGnReducers * ntw + apps), (size_t)st * sb, ntw};
     return true;
   }
   return false;
@@ -914,9 +895,8 @@ bool pick_pipe_min(int nvec, bool bwd, int min_stages, PipeShape* ps) {
 
 // The smallest cluster with three stages: measured on GB300, larger
 // clusters with deeper rings are slower (fewer resident clusters, costlier
-// exchanges), e.g. the (16, 512, 64, 64) backward takes 101 us with six
-// stages in clusters of 8 against 63 us with three in clusters of 4.
-bool pick_pipe(int nvec, bool bwd, PipeShape* ps) { return pick_pipe_min(nvec, bwd, 3, ps); }
+// exchanges).
+bool pick_pipe(int nvec, PipeShape* ps) { return pick_pipe_min(nvec, 3, ps); }
 
 // Whether clusters of `csize` CTAs of `block` threads of `kern` can be
 // resident on the current device (some sizes above 8 cannot), cached.
@@ -1028,6 +1008,48 @@ int pipe_clusters(const void* kern, const PipeShape& ps) {
   return n;
 }
 
+// Shape of the L2-staged backward: among the power-of-two clusters (1..16)
+// that divide the group's vectors and leave at most kL2MaxVec a CTA, those
+// whose in-flight slices (two groups of x and dy a CTA, over every resident
+// CTA) fit in kL2Budget bytes of L2; of these the fewest rounds of groups
+// times (slice + a fixed cost a group for its barriers and exchange), the
+// smaller cluster on a tie.  The ring takes what shared memory the per-vector
+// sums leave (at least three stages).  False when none fits.
+constexpr size_t kL2Budget = (size_t)96 << 20;
+constexpr int kL2GroupCost = 1024;  // in slice vectors
+
+struct L2Shape {
+  int csize, nv, stages;
+  int64_t ncl;
+  size_t smem;
+};
+
+template <typename T>
+bool pick_l2(int nvec, int64_t groups, L2Shape* out) {
+  const void* kern = (const void*)gn_bwd_l2<T>;
+  const size_t stride = (size_t)2 * kL2Chunk * 16;
+  int64_t best = -1;
+  for (int k = 1; k <= kMaxCluster; k *= 2) {
+    if (nvec % k || nvec / k > kL2MaxVec) continue;
+    const int nv = nvec / k;
+    const size_t vs = (size_t)nv * sizeof(float2);
+    int stages = (int)(((size_t)kGnSmem - vs) / stride);
+    if (stages > kL2Stages) stages = kL2Stages;
+    if (stages < 3) continue;
+    const size_t smem = (size_t)stages * stride + vs;
+    const int64_t active = pipe_clusters(kern, PipeShape{k, stages, nv, kL2Threads, smem, 0});
+    if (active <= 0) continue;
+    if ((size_t)4 * nv * 16 * (size_t)(active * k) > kL2Budget) continue;
+    const int64_t ncl = active < groups ? active : groups;
+    const int64_t cost = (groups + ncl - 1) / ncl * (nv + kL2GroupCost);
+    if (best < 0 || cost < best) {
+      best = cost;
+      *out = L2Shape{k, nv, stages, ncl, smem};
+    }
+  }
+  return best >= 0;
+}
+
 // Slices of at most 2048 vectors where a cluster of 16 allows it (about 64
 // registers a thread: two CTAs of 512 threads per SM, so that one CTA's
 // loads overlap another's reductions and stores), else up to 4096.
@@ -1052,7 +1074,7 @@ cudaError_t gn_fwd_t(const GnArgs& a, cudaStream_t s) {
   if (a.vec_ok) {
     const int nvec = M / E;
     PipeShape ps;
-    if (pick_pipe(nvec, false, &ps)) {
+    if (pick_pipe(nvec, &ps)) {
       auto kern = gn_fwd_pipe<T>;
       const int64_t active = pipe_clusters((const void*)kern, ps);
       if (active > 0) {
@@ -1095,35 +1117,12 @@ cudaError_t gn_bwd_t(const GnArgs& a, cudaStream_t s, int* launches) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int csize = 0;
-  PipeShape ps;
-  if (a.vec_ok && pick_pipe(M / E, true, &ps)) {
-    auto kern = gn_bwd_pipe<T>;
-    const int64_t active = pipe_clusters((const void*)kern, ps);
-    if (active > 0) {
-      const int64_t ncl = active < groups ? active : groups;
-      csize = ps.csize;
-      e = launch_kernel(kern, dim3((unsigned)(ncl * ps.csize)), dim3(ps.threads), ps.smem, s,
-                        ps.csize, dy, x, g, a.mean, a.rstd, dx, a.partial, groups, M,
-                        a.spatial / E, Cg, a.groups, a.channels, ps.csize, ps.stages, ps.nv,
-                        ps.ntw);
-    }
-  }
-  if (csize == 0 && a.vec_ok) {
-    const int nvec = M / E;
-    for (int cs = pick_gn_size(nvec, groups, sm_count(dev));
-         cs >= 1 && nvec / cs <= kGnMaxVec && groups * cs <= 0x7fffffff; cs /= 2) {
-      const int nv = nvec / cs;
-      const int vpt = gn_vpt(nv);
-      const unsigned threads = (unsigned)(((nv + vpt - 1) / vpt + 31) / 32 * 32);
-      auto kern = vpt == 1 ? gn_bwd_cluster<T, 1> : vpt == 2 ? gn_bwd_cluster<T, 2>
-                : vpt == 4 ? gn_bwd_cluster<T, 4> : gn_bwd_cluster<T, 8>;
-      if (!cluster_fits((const void*)kern, (int)threads, cs)) continue;
-      csize = cs;
-      e = launch_clustered(kern, (unsigned)(groups * cs), threads, cs, s, dy, x, g, a.mean,
-                           a.rstd, dx, a.partial, M, a.spatial / E, Cg, a.groups, a.channels,
-                           cs);
-      break;
-    }
+  L2Shape ls;
+  if (a.vec_ok && pick_l2<T>(M / E, groups, &ls)) {
+    csize = ls.csize;
+    e = launch_kernel(gn_bwd_l2<T>, dim3((unsigned)(ls.ncl * ls.csize)), dim3(kL2Threads),
+                      ls.smem, s, ls.csize, dy, x, g, a.mean, a.rstd, dx, a.partial, groups, M,
+                      a.spatial / E, Cg, a.groups, a.channels, ls.csize, ls.nv, ls.stages);
   }
   if (csize == 0) {
     csize = 1;

@@ -94,9 +94,9 @@ def test_softmax_dispatch(L):
 
 
 def test_group_norm_dispatch(L):
-    for name, fwd, bwd in (("gn_bf16_16x32x256x256_g8", "gn_fwd_pipe", "gn_bwd_pipe"),
-                           ("gn_bf16_16x512x64x64_g32", "gn_fwd_pipe", "gn_bwd_pipe"),
-                           ("gn_fp32_16x32x256x256_g8", "gn_fwd_pipe", "gn_bwd_cluster")):
+    for name, fwd, bwd in (("gn_bf16_16x32x256x256_g8", "gn_fwd_pipe", "gn_bwd_l2"),
+                           ("gn_bf16_16x512x64x64_g32", "gn_fwd_pipe", "gn_bwd_l2"),
+                           ("gn_fp32_16x32x256x256_g8", "gn_fwd_pipe", "gn_bwd_l2")):
         w = W.group_norm_workloads()[name]
         t = _dev(w, rows=2)
         _, m, r = L.group_norm_fwd(t["x"], t["gamma"], t["beta"], w.groups, w.eps)
