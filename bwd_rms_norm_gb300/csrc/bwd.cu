@@ -189,29 +189,34 @@ __global__ void __launch_bounds__(256) bwd_scalar(
 
 // out[j] = sum_b partial[b][j] over the `ncols` columns of a [nparts, ncols]
 // fp32 matrix, written to out0[j] for j < split and to out1[j - split]
-// otherwise.  Block (32 columns) x (32 lanes over b): lane t sums b = t,
-// t+32, ... in increasing order, then lane 0 adds the 32 lane sums in order.
-// The order depends only on nparts.
-__global__ void __launch_bounds__(1024) dw_finalize(const float* __restrict__ partial,
-                                                    int nparts, int ncols,
-                                                    float* __restrict__ out0,
-                                                    float* __restrict__ out1, int split) {
+// otherwise.  Block (32 columns) x (kFinLanes lanes over b): lane t sums
+// b = t, t + kFinLanes, ... in increasing order, then lane 0 adds the lane
+// sums in order.  The order depends only on nparts.  Blocks of 512 threads
+// fit beside a resident CTA of the row kernel, so they are already waiting
+// when it finishes (programmatic dependent launch); measured on GB300, 8
+// lanes are slower (longer serial sums) and 32 no faster.
+constexpr int kFinLanes = 16;
+
+__global__ void __launch_bounds__(32 * kFinLanes) dw_finalize(const float* __restrict__ partial,
+                                                             int nparts, int ncols,
+                                                             float* __restrict__ out0,
+                                                             float* __restrict__ out1, int split) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float s[32][33];
+  __shared__ float s[kFinLanes][33];
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int j = blockIdx.x * 32 + tx;
   float a = 0.f;
   if (j < ncols) {
-#pragma unroll 4
-    for (int b = ty; b < nparts; b += 32) a += partial[(int64_t)b * ncols + j];
+#pragma unroll 8
+    for (int b = ty; b < nparts; b += kFinLanes) a += partial[(int64_t)b * ncols + j];
   }
   s[ty][tx] = a;
   __syncthreads();
   if (ty == 0 && j < ncols) {
     float t = 0.f;
 #pragma unroll
-    for (int q = 0; q < 32; ++q) t += s[q][tx];
+    for (int q = 0; q < kFinLanes; ++q) t += s[q][tx];
     if (j < split)
       out0[j] = t;
     else if (out1 != nullptr)
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(1024) dw_finalize(const float* __restrict__ pa
 
 cudaError_t launch_column_sums(const float* partial, int nparts, int ncols, float* out0,
                                float* out1, int split, cudaStream_t s) {
-  return launch_kernel(dw_finalize, dim3((unsigned)((ncols + 31) / 32)), dim3(32, 32), 0, s, 1,
+  return launch_kernel(dw_finalize, dim3((unsigned)((ncols + 31) / 32)), dim3(32, kFinLanes), 0, s, 1,
                        partial, nparts, ncols, out0, out1, split);
 }
 
