@@ -991,60 +991,63 @@ cudaError_t launch_bwd_tma_v(const BwdArgs& a, int appliers, int stages, int red
                        a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers);
 }
 
-// Backward for rows of 4096 vectors (32768 16-bit or 16384 fp32 elements)
-// over a cluster of two CTAs: CTA q of the pair stages, reduces and writes
-// columns [q * N/2, (q+1) * N/2) of every row of the pair's contiguous row
-// range, so a ring stage (its halves of x and dy) is 64 KB and three fit.
-// The roles are those of bwd_tma_wide (reducer teams of kWideTeam warps,
-// appliers of four vectors with packed gains); a team's half-row dot is
-// exchanged with the peer CTA through distributed shared memory -- the
-// team's first warp stores it into the peer's slot and arrives on the
-// peer's exchange mbarrier -- and both CTAs add the two halves in rank
-// order.  Exchange slots are double-buffered per team (the peer cannot
-// start the team's row after next before this CTA has read the current
-// one: that row needs this CTA's next half).  Every CTA ends with a cluster
-// barrier so that no CTA exits while its peer may still store into it.
-template <typename T>
-__global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_pair(
+// Backward for wide rows over a cluster of csize (2 or 4) CTAs: CTA q of
+// the cluster stages, reduces and writes columns [q * N/csize, (q+1) *
+// N/csize) of every row of the cluster's contiguous row range, so that a
+// ring stage (its parts of x and dy) is small enough for six stages and
+// more.  The roles are those of bwd_tma_wide (reducer teams of kWideTeam
+// warps, appliers of four vectors with packed gains); a team's part of the
+// row dot goes to every CTA of the cluster through distributed shared
+// memory -- the team's first warp stores it into each CTA's slot and
+// arrives on that CTA's exchange mbarrier -- and every CTA adds the parts
+// in rank order.  Exchange slots are double-buffered per team (no CTA can
+// start the team's row after next before every CTA has read the current
+// one: that row needs every CTA's part of the next).  Every CTA ends with a
+// cluster barrier so that no CTA exits while a peer may still store into it.
+constexpr int kMaxSplit = 4;
+
+template <typename T, int CS>
+__global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
     int64_t rows, int hidden, float off, int stages, int reducers) {
+  constexpr int csize = CS;
   constexpr int E = Traits<T>::kVec;
   constexpr int VPT = 4;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Pipe pipe;
   __shared__ uint64_t xbar[3][2];
-  __shared__ float xch[3][2][2];
+  __shared__ float xch[3][2][CS];
   __shared__ float tred[3][2][kWideTeam];
   const uint32_t rank = cta_rank();
-  const int half = hidden / 2;               // columns a CTA owns
-  const int half_bytes = half * (int)sizeof(T);
-  const int stride = (2 * half_bytes + 127) / 128 * 128;
+  const int part = hidden / csize;           // columns a CTA owns
+  const int part_bytes = part * (int)sizeof(T);
+  const int stride = (2 * part_bytes + 127) / 128 * 128;
   unsigned char* ring = smem;
   const int appliers = blockDim.x - 32 * (1 + reducers * kWideTeam);
-  const int64_t cid = blockIdx.x / 2, ncl = gridDim.x / 2;
+  const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
   Rows rw;
   rw.r0 = cid * rows / ncl;
   rw.n = (int)((cid + 1) * rows / ncl - rw.r0);
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
-  if (threadIdx.x < 6) mbar_init(&xbar[threadIdx.x / 2][threadIdx.x % 2], 2);
+  if (threadIdx.x < 6) mbar_init(&xbar[threadIdx.x / 2][threadIdx.x % 2], csize);
   fence_mbar_init();
   __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised
+  cluster_sync();  // the peers' barriers are initialised
   pdl_trigger();
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvec = half / E;                 // vectors of this CTA's columns
-  const int doff = half_bytes / 16;
-  const int64_t col0 = (int64_t)rank * half; // first column of this CTA
+  const int nvec = part / E;                 // vectors of this CTA's columns
+  const int doff = part_bytes / 16;
+  const int64_t col0 = (int64_t)rank * part; // first column of this CTA
 
   if (warp == 0) {
     if (lane == 0) {
       const void* const src[2] = {x + col0, dy + col0};
       produce_pitched<2>(pipe, ring, stride, stages, src, rw, (size_t)hidden * sizeof(T),
-                         (uint32_t)half_bytes, abort);
+                         (uint32_t)part_bytes, abort);
     }
   } else if (warp <= reducers * kWideTeam) {
     const int d = (warp - 1) / kWideTeam, tw = (warp - 1) % kWideTeam;
@@ -1069,28 +1072,28 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_pair(
           : "memory");
       if (!all_ok) break;
       const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
-      float part[E];
+      float acc[E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) part[e] = 0.f;
+      for (int e = 0; e < E; ++e) acc[e] = 0.f;
       for (int v = tw * 32 + lane; v < nvec; v += nthr) {
         float xf[E], df[E], gf[E];
         unpack<T>(st[v], xf);
         unpack<T>(st[doff + v], df);
         unpack<T>(ld_shared_ro(gamma + col0 + (int64_t)v * E), gf);
 #pragma unroll
-        for (int e = 0; e < E; ++e) part[e] = fmaf(df[e] * (gf[e] + off), xf[e], part[e]);
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(df[e] * (gf[e] + off), xf[e], acc[e]);
       }
-      const float wdot = warp_sum(pairwise<E>(part));
+      const float wdot = warp_sum(pairwise<E>(acc));
       float* slot = tred[d][tpar];
       tpar ^= 1;
       if (lane == 0) slot[tw] = wdot;
       asm volatile("bar.sync %0, %1;" ::"r"(2 + d), "r"(nthr) : "memory");
       if (tw == 0) {
-        float half_dot = 0.f;
-        for (int w = 0; w < kWideTeam; ++w) half_dot += slot[w];
-        // send this CTA's half to both CTAs of the pair (itself included)
-        if (lane < 2) {
-          st_peer(&xch[d][par][rank], (uint32_t)lane, half_dot);
+        float mine = 0.f;
+        for (int w = 0; w < kWideTeam; ++w) mine += slot[w];
+        // send this CTA's part to every CTA of the cluster (itself included)
+        if (lane < csize) {
+          st_peer(&xch[d][par][rank], (uint32_t)lane, mine);
           mbar_arrive_peer(&xbar[d][par], (uint32_t)lane);
         }
         prev_ok = __all_sync(0xffffffffu,
@@ -1098,7 +1101,10 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_pair(
                                                   &g_wait_timeouts));
         if (prev_ok) {
           if (par) xph1 ^= 1u; else xph0 ^= 1u;
-          const float dot = (xch[d][par][0] + xch[d][par][1]) * rs;
+          float dot = 0.f;
+#pragma unroll
+          for (int r = 0; r < csize; ++r) dot += xch[d][par][r];
+          dot *= rs;
           par ^= 1;
           if (lane == 0) {
             pipe.stat[pos.stage] = dot / (float)hidden;
@@ -1173,33 +1179,47 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_pair(
   cluster_sync();  // no peer stores into this CTA after it exits
 }
 
-// The paired backward: pairs of CTAs, each three 64 KB stages of half rows;
-// false when the half rows do not fit that shape.
+// The split backward: clusters of csize CTAs, the smallest csize (2 or 4)
+// whose parts of a row leave at least min_stages ring stages (a multiple of
+// the three reducer teams), else the largest that leaves three.  Measured
+// on GB300: fp32 rows gain from six stages (16384 fp32: 0.78 of the copy
+// bandwidth in clusters of 4 against 0.69 in pairs), 16-bit rows do not
+// (32768 fp16: 0.64 in pairs with three stages, 0.62 in clusters of 4 with
+// six), having twice the arithmetic per staged byte.  False when none fits.
+
 template <typename T>
-bool try_bwd_pair_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
   constexpr int E = Traits<T>::kVec;
-  if (a.hidden % (2 * E)) return false;
-  const int half_bytes = a.hidden / 2 * (int)sizeof(T);
-  const int stride = (2 * half_bytes + 127) / 128 * 128;
-  const int stages = kRingBudget / stride >= 3 ? 3 : 0, reducers = 3;
-  if (stages < 3) return false;
-  int appliers = 0;
-  if (pick_vpt(a.hidden / 2 / E, kWideThreads - 32 * (1 + reducers * kWideTeam), 4,
-               &appliers) != 4)
-    return false;
+  const int reducers = 3;
+  const int min_stages = sizeof(T) == 4 ? 6 : 3;
+  int csize = 0, stages = 0, appliers = 0;
+  for (int k = 2; k <= kMaxSplit; k *= 2) {
+    if (a.hidden % (k * E)) continue;
+    const int stride = (2 * (a.hidden / k) * (int)sizeof(T) + 127) / 128 * 128;
+    int st = kRingBudget / stride;
+    if (st > kMaxStages) st = kMaxStages;
+    st -= st % reducers;
+    // four vectors an applier (the kernel's packed gains)
+    const int app = ((a.hidden / k / E + 3) / 4 + 31) / 32 * 32;
+    if (st < 3 || app > kWideThreads - 32 * (1 + reducers * kWideTeam)) continue;
+    csize = k;
+    stages = st;
+    appliers = app;
+    if (st >= min_stages) break;
+  }
+  if (csize == 0) return false;
+  const int stride = (2 * (a.hidden / csize) * (int)sizeof(T) + 127) / 128 * 128;
   const int threads = 32 * (1 + reducers * kWideTeam) + appliers;
-  auto kern = bwd_tma_pair<T>;
+  auto kern = csize == 2 ? bwd_tma_split<T, 2> : bwd_tma_split<T, 4>;
   if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
-  int dev = 0;
-  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return true;
-  // as many pairs as can be resident at once (one CTA per SM)
+  // as many clusters as can be resident at once (one CTA per SM)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
+  cfg.gridDim = dim3((unsigned)csize);
   cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = (size_t)stages * stride;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = (unsigned)csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -1209,12 +1229,12 @@ bool try_bwd_pair_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* npa
     cudaGetLastError();
     return false;
   }
-  int64_t pairs = active;
-  if (pairs > a.rows) pairs = a.rows;
-  if (pairs > a.max_partials) pairs = a.max_partials;
-  *nparts = (int)pairs;
-  *err = launch_kernel(kern, dim3((unsigned)(2 * pairs)), dim3(threads), (size_t)stages * stride,
-                       s, 2, static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
+  int64_t ncl = active;
+  if (ncl > a.rows) ncl = a.rows;
+  if (ncl > a.max_partials) ncl = a.max_partials;
+  *nparts = (int)ncl;
+  *err = launch_kernel(kern, dim3((unsigned)(csize * ncl)), dim3(threads), (size_t)stages * stride,
+                       s, csize, static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
                        static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
                        a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers);
   return true;
@@ -1257,7 +1277,7 @@ bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* npar
   const int vpt = stages < 3 ? 0
                              : pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 2,
                                         &appliers);
-  if (vpt == 0) return try_bwd_wide_t<T>(a, s, err, nparts) || try_bwd_pair_t<T>(a, s, err, nparts);
+  if (vpt == 0) return try_bwd_wide_t<T>(a, s, err, nparts) || try_bwd_split_t<T>(a, s, err, nparts);
   const int grid = grid_for(a.rows, a.max_partials, err);
   if (*err != cudaSuccess) return true;
   *nparts = grid;

@@ -39,7 +39,7 @@ RMS = [  # workload, forward kernel, backward row kernel
     ("fp16_4096x2048", "fwd_cta_row", "bwd_tma"),
     ("fp16_4096x8192", "fwd_tma", "bwd_tma"),
     ("fp16_4096x16384", "fwd_tma", "bwd_tma_wide"),
-    ("fp16_4096x32768", "fwd_cta_row", "bwd_tma_pair"),
+    ("fp16_4096x32768", "fwd_cta_row", "bwd_tma_split"),
     ("large_bf16_16384x8192_once", "fwd_tma", "bwd_tma"),
     ("fp32_256x1024", "fwd_cta_row", "bwd_tma"),
 ]
