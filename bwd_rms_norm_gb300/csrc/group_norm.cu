@@ -1117,7 +1117,7 @@ cudaError_t gn_bwd_t(const GnArgs& a, cudaStream_t s, int* launches) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int csize = 0;
-  L2Shape ls;
+  L2Shape ls{};
   if (a.vec_ok && pick_l2<T>(M / E, groups, &ls)) {
     csize = ls.csize;
     e = launch_kernel(gn_bwd_l2<T>, dim3((unsigned)(ls.ncl * ls.csize)), dim3(kL2Threads),
