@@ -24,6 +24,10 @@ The functions carry the names of the C entry points declared in
   ``(dx, dgamma, dbeta)`` (x of shape [n, channels, *spatial])
 * ``layer_norm_fwd(x, gamma, beta, eps)`` -> ``(y, mean, rstd)``
 * ``layer_norm_bwd(dy, x, gamma, mean, rstd)`` -> ``(dx, dgamma, dbeta)``
+
+For autograd: ``rms_norm(x, weight, eps, offset=0, cast_mode="round_once")``
+(a ``torch.autograd.Function`` over rms_norm_fwd / rms_norm_bwd) and the
+module ``RMSNorm(hidden, eps, offset=0, cast_mode="round_once")``.
 """
 from __future__ import annotations
 
@@ -505,3 +509,54 @@ def group_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean:
     if st != RMSN_OK:
         raise RMSNormError("group_norm_bwd", st)
     return dx, dgamma, (dbeta if with_dbeta else None)
+
+
+class RMSNormFunction(torch.autograd.Function):
+    """RMSNorm over the last dimension with this library's forward and
+    backward.  The backward's weight gradient, summed in fp32 by the library,
+    is cast to the weight's dtype (autograd wants the parameter's dtype)."""
+
+    @staticmethod
+    def forward(ctx, x, weight, eps, offset, cast_mode):
+        x = x.contiguous()
+        weight = weight.contiguous()
+        y, rstd = rms_norm_fwd(x, weight, eps, offset, cast_mode)
+        ctx.save_for_backward(x, weight, rstd)
+        ctx.offset = offset
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, weight, rstd = ctx.saved_tensors
+        dx, dw = rms_norm_bwd(dy.contiguous(), x, weight, rstd, ctx.offset)
+        return dx, dw.to(weight.dtype), None, None, None
+
+
+def rms_norm(x: torch.Tensor, weight: torch.Tensor, eps: float, offset: int = 0,
+             cast_mode: str = "round_once") -> torch.Tensor:
+    """Differentiable RMSNorm of ``x`` over its last dimension (gain
+    ``weight``, or ``1 + weight`` with ``offset=1``)."""
+    return RMSNormFunction.apply(x, weight, eps, offset, cast_mode)
+
+
+class RMSNorm(torch.nn.Module):
+    """RMSNorm layer over the last dimension of its input.  The weight starts
+    at 1 (gain ``weight``) or at 0 with ``offset=1`` (gain ``1 + weight``)."""
+
+    def __init__(self, hidden: int, eps: float = 1e-6, offset: int = 0,
+                 cast_mode: str = "round_once", device=None, dtype=None):
+        super().__init__()
+        if offset not in (0, 1):
+            raise ValueError("offset must be 0 or 1")
+        if cast_mode not in CAST_MODES:
+            raise ValueError(f"cast_mode must be one of {sorted(CAST_MODES)}")
+        self.weight = torch.nn.Parameter(
+            torch.full((hidden,), 0.0 if offset else 1.0, device=device, dtype=dtype))
+        self.eps, self.offset, self.cast_mode = eps, offset, cast_mode
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        return rms_norm(x, self.weight, self.eps, self.offset, self.cast_mode)
+
+    def extra_repr(self) -> str:
+        return (f"{self.weight.numel()}, eps={self.eps}, offset={self.offset}, "
+                f"cast_mode={self.cast_mode!r}")

@@ -227,3 +227,20 @@ def test_last_kernels_without_launches(lib):
     assert fwd(lib, dtype=3) == 4
     assert lib.rms_norm_last_kernels(names, 4) == 0
     assert lib.rms_norm_last_kernels(None, 4) < 0
+
+
+def test_rms_norm_module_host_side():
+    """The autograd layer builds its weight on the host, checks its
+    arguments, and refuses CPU inputs like every other call."""
+    import torch
+    import bwd_rms_norm_gb300 as L
+    m = L.RMSNorm(16, eps=1e-5)
+    assert torch.equal(m.weight.detach(), torch.ones(16))
+    g = L.RMSNorm(16, offset=1, dtype=torch.bfloat16)
+    assert g.weight.dtype == torch.bfloat16 and torch.count_nonzero(g.weight).item() == 0
+    with pytest.raises(ValueError):
+        L.RMSNorm(16, offset=2)
+    with pytest.raises(ValueError):
+        L.RMSNorm(16, cast_mode="round_thrice")
+    with pytest.raises(RuntimeError, match="CUDA"):
+        m(torch.zeros(3, 16, requires_grad=True))
