@@ -38,6 +38,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -634,16 +635,25 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
                        "and copies out on three streams over two device buffer sets")}
 
 
+def code_of(text: str) -> str:
+    """C/C++/CUDA source with its comments removed and its whitespace
+    collapsed: what decides the kernels built from it."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def sources_hash(files) -> str:
-    """First 16 hex digits of the SHA-256 of the named CUDA sources (file
-    names and contents, in the given order), to tell whether committed
-    counters still describe the kernels being run."""
+    """First 16 hex digits of the SHA-256 of the named CUDA sources' code
+    (file names and code_of of their contents, in the given order), to
+    tell whether committed counters still describe the kernels being run;
+    edits to comments or layout leave it unchanged."""
     import hashlib
     h = hashlib.sha256()
     for name in files:
         h.update(name.encode())
-        with open(os.path.join(ROOT, "bwd_rms_norm_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "bwd_rms_norm_gb300", "csrc", name)) as fh:
+            h.update(code_of(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -5,13 +5,16 @@
 // write any output of a row before the whole row has been reduced, so two
 // things decide the speed: how many bytes each SM keeps in flight, and that
 // the latency of each row's reduction never stalls the stream of outputs.
-// One CTA per SM owns a contiguous range of rows and splits its warps into
-// three roles that meet at per-stage mbarriers:
+// One CTA per SM owns a contiguous range of rows (rows too wide for one
+// CTA's ring are split over a cluster of 2 or 4 CTAs, each staging its part
+// of every row) and splits its warps into three roles that meet at
+// per-stage mbarriers:
 //
 //   producer (warp 0, one thread)  streams the CTA's rows into a ring of
 //       shared-memory stages with 1D bulk copies (cp.async.bulk, the TMA
-//       engine) -- 8 to 32 stages, i.e. 100-200 KB of reads in flight per SM
-//       without any of it held in registers;                     -> full[s]
+//       engine) -- up to 96 KB of rows in flight per SM in the forward of
+//       rows up to 16 KB, up to 200 KB otherwise, none of it held in
+//       registers;                                                -> full[s]
 //   reducers (warps 1..R)  one warp per row (warp d takes the CTA's rows
 //       d, d + R, ...): the row statistic -- rstd in the forward,
 //       c = sum(g * x_hat) / hidden in the backward -- into the stage's slot;

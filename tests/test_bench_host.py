@@ -58,8 +58,9 @@ def test_every_workload_resolves_with_its_metric():
 
 
 def test_traffic_records_go_stale_with_their_sources(tmp_path, monkeypatch):
-    """A committed DRAM-traffic record is used only while the CUDA sources it
-    lists hash to the recorded value."""
+    """A committed DRAM-traffic record is used only while the code of the
+    CUDA sources it lists (comments and whitespace aside) hashes to the
+    recorded value."""
     csrc = tmp_path / "bwd_rms_norm_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
@@ -72,7 +73,11 @@ def test_traffic_records_go_stale_with_their_sources(tmp_path, monkeypatch):
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     assert bench.load_traffic("w")["bwd"] == 20
     assert bench.load_traffic("other") == {}
-    (csrc / "b.cuh").write_text("// helpers, changed\n")
+    # comments and layout do not change the kernels: the record stands
+    (csrc / "a.cu").write_text("/* the kernel */\n__global__  void k()\n{}  // empty\n")
+    assert bench.load_traffic("w")["bwd"] == 20
+    # code does: the record is dropped
+    (csrc / "b.cuh").write_text("#define HELPER 1\n")
     assert bench.load_traffic("w") == {}
 
 
