@@ -1,8 +1,9 @@
 // Wide-row forward and backward kernels for sm_103a: thread-block clusters.
 //
-// A row of 32768 or 65536 elements is too wide for one CTA to hold in
-// registers (and, in the backward, x and dy of one row fill the shared
-// memory a staged ring would need for several rows).  Here a row is split
+// The widest rows (65536 fp32: 256 KB of x, twice that with dy) are too
+// wide for one CTA to hold in registers and for the staged kernels' rings,
+// even split over a cluster of 4 (the narrower wide rows take those).  Here
+// a row is split
 // over the C CTAs of a cluster (C = 2, 4, 8 or 16): CTA rank q owns columns
 // [q*N/C, (q+1)*N/C), holds its slice in registers, reduces it (warp
 // shuffles, then the CTA's warps in order), and pushes the CTA's partial sum
