@@ -6,7 +6,6 @@ import torch
 
 import workloads as W
 from oracle import fp8 as of8
-from oracle import rms_norm as orm
 
 import parity as P
 
@@ -45,8 +44,7 @@ def run_and_check(L, w, scale, sample_limit=1024, to_dev=None):
     rows = _sample_rows(w.rows, sample_limit)
     ref, rstd_ref = of8.forward_fp8(xd[rows], gd, w.eps, w.offset, scale)
     P.check_rstd(rstd.cpu().numpy()[rows], rstd_ref)
-    y_exact, _ = orm.forward_exact(xd[rows], gd, w.eps, w.offset)
-    P.check_rows(_y8_values(y8)[rows], ref, "e4m3", None, "y8", y_exact * scale)
+    P.check_rows(_y8_values(y8)[rows], ref, "e4m3", None, "y8")
     # the rstd of the storage-type forward: bit-identical where the same
     # kernel runs (every width but the fp32 rows that only a cluster holds,
     # where the FP8 store takes the scalar kernel and sums in another order)
@@ -130,9 +128,7 @@ def test_fp8_scale_is_read_on_the_device(L):
         torch.cuda.synchronize()
         ref, _ = of8.forward_fp8(W.as_float64(inp["x"]), W.as_float64(inp["gamma"]), w.eps, 0,
                                  scale)
-        y_exact, _ = orm.forward_exact(W.as_float64(inp["x"]), W.as_float64(inp["gamma"]),
-                                       w.eps, 0)
-        P.check_rows(_y8_values(y8), ref, "e4m3", None, "y8", y_exact * scale)
+        P.check_rows(_y8_values(y8), ref, "e4m3", None, "y8")
 
 
 def test_fp8_backward_runs_on_its_rstd(L):

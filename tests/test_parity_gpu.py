@@ -70,7 +70,8 @@ def run_and_check(L, w: W.Workload, sample_limit: int = 1024, inputs=None, to_de
     dx_got = W.as_float64(dx.cpu())[rows]
     terms = rstd_ref[rows, None] * dyd[rows] * orm.gain(gd, w.offset)[None, :]
     stats.update({"dx_" + k: v for k, v in
-                  P.check_rows(dx_got, dx_ref, fmt, None, "dx", terms).items()})
+                  P.check_rows(dx_got, dx_ref, fmt, None, "dx", terms,
+                                cancels=True).items()})
     stats.update(P.check_dw(dw.cpu().numpy(), dw_ref))
     return stats
 

@@ -53,7 +53,7 @@ def run_and_check(L, w, to_dev=None, bias=True, sample_limit=4):
         terms = terms + np.abs(bd)[None, :, None]
     terms = _rows(terms, k, G)
     P.check_rows(_rows(W.as_float64(y[:k].cpu()), k, G), _rows(y_ref, k, G), fmt, None, "y",
-                 terms)
+                 terms, cancels=True)
 
     m_in = rounding.round_to(mean_ex, "f32")
     r_in = rounding.round_to(rstd_ex, "f32")
@@ -66,7 +66,7 @@ def run_and_check(L, w, to_dev=None, bias=True, sample_limit=4):
                                                               axis=1)[:, :, None]
     P.check_rows(_rows(W.as_float64(dx[:k].cpu()), k, G),
                  _rows(rounding.round_to(dx_ex[:k], fmt), k, G), fmt, None, "dx",
-                 _rows(dterms, k, G))
+                 _rows(dterms, k, G), cancels=True)
     P.check_dw(dgam.cpu().numpy(), rounding.round_to(dg_ex, "f32"))
     P.check_dw(dbet.cpu().numpy(), rounding.round_to(db_ex, "f32"))
     return dx, dgam, dbet

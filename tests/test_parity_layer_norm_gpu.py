@@ -51,7 +51,7 @@ def run_and_check(L, w, sample_limit=1024, bias=True, to_dev=None):
     y_ref, _, _ = oln.forward(xd[rows], gd, bd, w.eps, fmt)
     x_hat = (xd[rows] - mean_ex[rows, None]) * rstd_ex[rows, None]
     terms = np.abs(x_hat * gd) + (np.abs(bd) if bd is not None else 0.0)
-    P.check_rows(W.as_float64(y.cpu())[rows], y_ref, fmt, None, "y", terms)
+    P.check_rows(W.as_float64(y.cpu())[rows], y_ref, fmt, None, "y", terms, cancels=True)
 
     m_in = to_dev(torch.from_numpy(mean_ref.astype(np.float32)))
     r_in = to_dev(torch.from_numpy(rstd_ref.astype(np.float32)))
@@ -60,7 +60,7 @@ def run_and_check(L, w, sample_limit=1024, bias=True, to_dev=None):
     dx_ex, dg_ex, db_ex = oln.backward_exact(dyd, xd, gd, mean_ref, rstd_ref)
     dterms = rstd_ref[rows, None] * dyd[rows] * gd[None, :]
     P.check_rows(W.as_float64(dx.cpu())[rows], rounding.round_to(dx_ex[rows], fmt), fmt, None,
-                 "dx", dterms)
+                 "dx", dterms, cancels=True)
     P.check_dw(dgam.cpu().numpy(), rounding.round_to(dg_ex, "f32"))
     P.check_dw(dbet.cpu().numpy(), rounding.round_to(db_ex, "f32"))
 
