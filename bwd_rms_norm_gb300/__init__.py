@@ -175,11 +175,43 @@ def _stream_handle(device: torch.device, stream: Optional[torch.cuda.Stream]) ->
     return s.cuda_stream
 
 
-def _check_cuda(name: str, t: torch.Tensor) -> None:
+def _check_cuda(name: str, t: torch.Tensor, device: Optional[torch.device] = None) -> None:
     if not t.is_cuda:
         raise RuntimeError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if device is not None and t.device != device:
+        raise RuntimeError(f"{name} is on {t.device}, the other tensors on {device}")
     if not t.is_contiguous():
         raise RuntimeError(f"{name} must be contiguous")
+
+
+def _check_like(name: str, t: Optional[torch.Tensor], dtype: torch.dtype, numel: int,
+                shape=None) -> None:
+    """A tensor the kernels read or write a fixed extent of: its dtype and
+    size are checked on the host before anything reaches the device (a short
+    buffer would be read or written out of bounds)."""
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise RuntimeError(f"{name} must be {dtype}, not {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise RuntimeError(f"{name} must have shape {tuple(shape)}, not {tuple(t.shape)}")
+    if t.numel() != numel:
+        raise RuntimeError(f"{name} must have {numel} elements, not {t.numel()}")
+
+
+def _check_bwd_args(dy, x, gamma, rstd, dx, dw) -> Tuple[int, int]:
+    """Host-side checks shared by the RMSNorm backward entry points: dtypes,
+    shapes and element counts of every tensor, caller-supplied outputs
+    included.  Returns (rows, hidden)."""
+    if x.dtype not in DTYPE_CODES:
+        raise RuntimeError(f"x must be float32, bfloat16 or float16, not {x.dtype}")
+    rows, hidden = _as_rows(x)
+    _check_like("dy", dy, x.dtype, x.numel(), x.shape)
+    _check_like("gamma", gamma, x.dtype, hidden)
+    _check_like("rstd", rstd, torch.float32, rows)
+    _check_like("dx", dx, x.dtype, x.numel(), x.shape)
+    _check_like("dw", dw, torch.float32, hidden)
+    return rows, hidden
 
 
 def _as_rows(x: torch.Tensor) -> Tuple[int, int]:
@@ -197,19 +229,22 @@ def rms_norm_fwd(x: torch.Tensor, gamma: torch.Tensor, eps: float, offset: int =
     """Forward over the last dimension of ``x``; returns ``(y, rstd)`` with
     ``y`` shaped like ``x`` and ``rstd`` fp32 of shape ``x.shape[:-1]``."""
     lib = load_library()
-    _check_cuda("x", x)
-    _check_cuda("gamma", gamma)
-    if gamma.dtype != x.dtype:
-        raise RuntimeError("gamma must have the dtype of x")
+    if x.dtype not in DTYPE_CODES:
+        raise RuntimeError(f"x must be float32, bfloat16 or float16, not {x.dtype}")
+    if cast_mode not in CAST_MODES:
+        raise RuntimeError(f"cast_mode must be one of {sorted(CAST_MODES)}")
     rows, hidden = _as_rows(x)
-    if gamma.numel() != hidden:
-        raise RuntimeError("gamma must have hidden elements")
+    _check_like("gamma", gamma, x.dtype, hidden)
+    _check_like("y", y, x.dtype, x.numel(), x.shape)
+    _check_like("rstd", rstd, torch.float32, rows)
+    _check_cuda("x", x)
+    _check_cuda("gamma", gamma, x.device)
     if y is None:
         y = torch.empty_like(x)
     if rstd is None:
         rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-    _check_cuda("y", y)
-    _check_cuda("rstd", rstd)
+    _check_cuda("y", y, x.device)
+    _check_cuda("rstd", rstd, x.device)
     with torch.cuda.device(x.device):
         st = lib.rms_norm_fwd(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), rows, hidden,
                               float(eps), int(offset), DTYPE_CODES[x.dtype],
@@ -231,24 +266,22 @@ def rms_norm_fwd_fp8(x: torch.Tensor, gamma: torch.Tensor, scale: torch.Tensor, 
     by the kernel); returns ``(y, rstd)`` with ``y`` of dtype
     torch.float8_e4m3fn shaped like ``x``."""
     lib = load_library()
-    _check_cuda("x", x)
-    _check_cuda("gamma", gamma)
-    _check_cuda("scale", scale)
-    if gamma.dtype != x.dtype:
-        raise RuntimeError("gamma must have the dtype of x")
-    if scale.dtype != torch.float32 or scale.numel() != 1:
-        raise RuntimeError("scale must be a one-element float32 tensor")
+    if x.dtype not in DTYPE_CODES:
+        raise RuntimeError(f"x must be float32, bfloat16 or float16, not {x.dtype}")
     rows, hidden = _as_rows(x)
-    if gamma.numel() != hidden:
-        raise RuntimeError("gamma must have hidden elements")
+    _check_like("gamma", gamma, x.dtype, hidden)
+    _check_like("scale", scale, torch.float32, 1)
+    _check_like("y", y, FP8_DTYPE, x.numel(), x.shape)
+    _check_like("rstd", rstd, torch.float32, rows)
+    _check_cuda("x", x)
+    _check_cuda("gamma", gamma, x.device)
+    _check_cuda("scale", scale, x.device)
     if y is None:
         y = torch.empty(x.shape, dtype=FP8_DTYPE, device=x.device)
-    if y.dtype != FP8_DTYPE or y.shape != x.shape:
-        raise RuntimeError("y must be a float8_e4m3fn tensor shaped like x")
     if rstd is None:
         rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-    _check_cuda("y", y)
-    _check_cuda("rstd", rstd)
+    _check_cuda("y", y, x.device)
+    _check_cuda("rstd", rstd, x.device)
     with torch.cuda.device(x.device):
         st = lib.rms_norm_fwd_fp8(_ptr(x), _ptr(gamma), _ptr(scale), _ptr(y), _ptr(rstd), rows,
                                   hidden, float(eps), int(offset), DTYPE_CODES[x.dtype],
@@ -266,17 +299,9 @@ def rms_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: t
     ``workspace`` (a byte or float tensor of at least
     ``rms_norm_bwd_workspace_size`` bytes) is allocated when not given."""
     lib = load_library()
-    for name, t in (("dy", dy), ("x", x), ("gamma", gamma), ("rstd", rstd)):
-        _check_cuda(name, t)
-    if dy.dtype != x.dtype or gamma.dtype != x.dtype:
-        raise RuntimeError("dy, x and gamma must share one dtype")
-    if rstd.dtype != torch.float32:
-        raise RuntimeError("rstd must be float32")
-    if dy.shape != x.shape:
-        raise RuntimeError("dy must have the shape of x")
-    rows, hidden = _as_rows(x)
-    if rstd.numel() != rows or gamma.numel() != hidden:
-        raise RuntimeError("rstd must have one value per row and gamma hidden values")
+    rows, hidden = _check_bwd_args(dy, x, gamma, rstd, dx, dw)
+    for name, t in (("x", x), ("dy", dy), ("gamma", gamma), ("rstd", rstd)):
+        _check_cuda(name, t, x.device)
     code = DTYPE_CODES[x.dtype]
     if dx is None:
         dx = torch.empty_like(x)
@@ -285,9 +310,9 @@ def rms_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, rstd: t
     need = int(lib.rms_norm_bwd_workspace_size(rows, hidden, code))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    _check_cuda("dx", dx)
-    _check_cuda("dw", dw)
-    _check_cuda("workspace", workspace)
+    _check_cuda("dx", dx, x.device)
+    _check_cuda("dw", dw, x.device)
+    _check_cuda("workspace", workspace, x.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(x.device):
         st = lib.rms_norm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dw),
@@ -308,15 +333,15 @@ def rms_norm_bwd_noalloc(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor,
     allocation on the Python side as well.  Calls that may overlap on the GPU
     share that array and must be ordered on one stream."""
     lib = load_library()
-    for name, t in (("dy", dy), ("x", x), ("gamma", gamma), ("rstd", rstd)):
-        _check_cuda(name, t)
-    if dy.dtype != x.dtype or gamma.dtype != x.dtype or rstd.dtype != torch.float32:
-        raise RuntimeError("dy, x, gamma share one dtype; rstd is float32")
-    rows, hidden = _as_rows(x)
+    rows, hidden = _check_bwd_args(dy, x, gamma, rstd, dx, dw)
+    for name, t in (("x", x), ("dy", dy), ("gamma", gamma), ("rstd", rstd)):
+        _check_cuda(name, t, x.device)
     if dx is None:
         dx = torch.empty_like(x)
     if dw is None:
         dw = torch.empty(hidden, dtype=torch.float32, device=x.device)
+    _check_cuda("dx", dx, x.device)
+    _check_cuda("dw", dw, x.device)
     with torch.cuda.device(x.device):
         st = lib.rms_norm_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx),
                                       _ptr(dw), rows, hidden, int(offset), DTYPE_CODES[x.dtype],
@@ -333,20 +358,23 @@ def layer_norm_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Te
     """LayerNorm forward over the last dimension; returns ``(y, mean, rstd)``
     (``beta`` may be None)."""
     lib = load_library()
-    _check_cuda("x", x)
-    _check_cuda("gamma", gamma)
-    if beta is not None:
-        _check_cuda("beta", beta)
-        if beta.dtype != x.dtype or beta.numel() != x.shape[-1]:
-            raise RuntimeError("beta must have the dtype of x and hidden elements")
-    if gamma.dtype != x.dtype:
-        raise RuntimeError("gamma must have the dtype of x")
+    if x.dtype not in DTYPE_CODES:
+        raise RuntimeError(f"x must be float32, bfloat16 or float16, not {x.dtype}")
     rows, hidden = _as_rows(x)
-    if gamma.numel() != hidden:
-        raise RuntimeError("gamma must have hidden elements")
+    _check_like("gamma", gamma, x.dtype, hidden)
+    _check_like("beta", beta, x.dtype, hidden)
+    _check_like("y", y, x.dtype, x.numel(), x.shape)
+    _check_like("mean", mean, torch.float32, rows)
+    _check_like("rstd", rstd, torch.float32, rows)
+    _check_cuda("x", x)
+    _check_cuda("gamma", gamma, x.device)
+    if beta is not None:
+        _check_cuda("beta", beta, x.device)
     y = torch.empty_like(x) if y is None else y
     mean = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if mean is None else mean
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device) if rstd is None else rstd
+    for name, t in (("y", y), ("mean", mean), ("rstd", rstd)):
+        _check_cuda(name, t, x.device)
     with torch.cuda.device(x.device):
         st = lib.layer_norm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
                                 rows, hidden, float(eps), DTYPE_CODES[x.dtype],
@@ -369,11 +397,11 @@ def layer_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean:
     """LayerNorm backward; returns ``(dx, dgamma, dbeta)`` (dbeta None when
     ``with_dbeta`` is False)."""
     lib = load_library()
-    for name, t in (("dy", dy), ("x", x), ("gamma", gamma), ("mean", mean), ("rstd", rstd)):
-        _check_cuda(name, t)
-    if dy.dtype != x.dtype or gamma.dtype != x.dtype:
-        raise RuntimeError("dy, x and gamma must share one dtype")
-    rows, hidden = _as_rows(x)
+    rows, hidden = _check_bwd_args(dy, x, gamma, rstd, dx, dgamma)
+    _check_like("mean", mean, torch.float32, rows)
+    _check_like("dbeta", dbeta if with_dbeta else None, torch.float32, hidden)
+    for name, t in (("x", x), ("dy", dy), ("gamma", gamma), ("mean", mean), ("rstd", rstd)):
+        _check_cuda(name, t, x.device)
     code = DTYPE_CODES[x.dtype]
     dx = torch.empty_like(x) if dx is None else dx
     dgamma = torch.empty(hidden, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
@@ -382,6 +410,10 @@ def layer_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean:
     need = int(lib.layer_norm_bwd_workspace_size(rows, hidden, code))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    for name, t in (("dx", dx), ("dgamma", dgamma), ("workspace", workspace)):
+        _check_cuda(name, t, x.device)
+    if with_dbeta:
+        _check_cuda("dbeta", dbeta, x.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(x.device):
         st = lib.layer_norm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),
@@ -398,12 +430,13 @@ def softmax_fwd(x: torch.Tensor, y: Optional[torch.Tensor] = None,
     """Softmax over the last dimension of ``x`` (fp32 arithmetic, one
     rounding to x's dtype at the store)."""
     lib = load_library()
-    _check_cuda("x", x)
+    if x.dtype not in DTYPE_CODES:
+        raise RuntimeError(f"x must be float32, bfloat16 or float16, not {x.dtype}")
     rows, cols = _as_rows(x)
+    _check_like("y", y, x.dtype, x.numel(), x.shape)
+    _check_cuda("x", x)
     y = torch.empty_like(x) if y is None else y
-    _check_cuda("y", y)
-    if y.dtype != x.dtype or y.shape != x.shape:
-        raise RuntimeError("y must match x in dtype and shape")
+    _check_cuda("y", y, x.device)
     with torch.cuda.device(x.device):
         st = lib.softmax_fwd(_ptr(x), _ptr(y), rows, cols, DTYPE_CODES[x.dtype],
                              _stream_handle(x.device, stream))
@@ -417,13 +450,15 @@ def softmax_bwd(dy: torch.Tensor, y: torch.Tensor, dx: Optional[torch.Tensor] = 
     """Backward of softmax_fwd from its output: dx = y * (dy - sum(dy * y))
     per row, the sum in fp32."""
     lib = load_library()
-    _check_cuda("dy", dy)
-    _check_cuda("y", y)
-    if dy.dtype != y.dtype or dy.shape != y.shape:
-        raise RuntimeError("dy and y must share dtype and shape")
+    if y.dtype not in DTYPE_CODES:
+        raise RuntimeError(f"y must be float32, bfloat16 or float16, not {y.dtype}")
     rows, cols = _as_rows(y)
+    _check_like("dy", dy, y.dtype, y.numel(), y.shape)
+    _check_like("dx", dx, y.dtype, y.numel(), y.shape)
+    _check_cuda("y", y)
+    _check_cuda("dy", dy, y.device)
     dx = torch.empty_like(y) if dx is None else dx
-    _check_cuda("dx", dx)
+    _check_cuda("dx", dx, y.device)
     with torch.cuda.device(y.device):
         st = lib.softmax_bwd(_ptr(dy), _ptr(y), _ptr(dx), rows, cols, DTYPE_CODES[y.dtype],
                              _stream_handle(y.device, stream))
@@ -451,18 +486,23 @@ def group_norm_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Te
     """GroupNorm forward over x [n, channels, *spatial]; returns ``(y, mean,
     rstd)`` with mean and rstd fp32 [n, groups] (``beta`` may be None)."""
     lib = load_library()
-    _check_cuda("x", x)
-    _check_cuda("gamma", gamma)
+    if x.dtype not in DTYPE_CODES:
+        raise RuntimeError(f"x must be float32, bfloat16 or float16, not {x.dtype}")
     n, c, sp = _gn_shape(x, groups)
-    if gamma.dtype != x.dtype or gamma.numel() != c:
-        raise RuntimeError("gamma must have the dtype of x and one value per channel")
+    _check_like("gamma", gamma, x.dtype, c)
+    _check_like("beta", beta, x.dtype, c)
+    _check_like("y", y, x.dtype, x.numel(), x.shape)
+    _check_like("mean", mean, torch.float32, n * groups)
+    _check_like("rstd", rstd, torch.float32, n * groups)
+    _check_cuda("x", x)
+    _check_cuda("gamma", gamma, x.device)
     if beta is not None:
-        _check_cuda("beta", beta)
-        if beta.dtype != x.dtype or beta.numel() != c:
-            raise RuntimeError("beta must have the dtype of x and one value per channel")
+        _check_cuda("beta", beta, x.device)
     y = torch.empty_like(x) if y is None else y
     mean = torch.empty(n, groups, dtype=torch.float32, device=x.device) if mean is None else mean
     rstd = torch.empty(n, groups, dtype=torch.float32, device=x.device) if rstd is None else rstd
+    for name, t in (("y", y), ("mean", mean), ("rstd", rstd)):
+        _check_cuda(name, t, x.device)
     with torch.cuda.device(x.device):
         st = lib.group_norm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
                                 n, c, sp, int(groups), float(eps), DTYPE_CODES[x.dtype],
@@ -487,11 +527,18 @@ def group_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean:
     """GroupNorm backward; returns ``(dx, dgamma, dbeta)`` (fp32 weight
     gradients; dbeta None when ``with_dbeta`` is False)."""
     lib = load_library()
-    for name, t in (("dy", dy), ("x", x), ("gamma", gamma), ("mean", mean), ("rstd", rstd)):
-        _check_cuda(name, t)
-    if dy.dtype != x.dtype or gamma.dtype != x.dtype or dy.shape != x.shape:
-        raise RuntimeError("dy, x and gamma must share one dtype; dy shaped like x")
+    if x.dtype not in DTYPE_CODES:
+        raise RuntimeError(f"x must be float32, bfloat16 or float16, not {x.dtype}")
     n, c, sp = _gn_shape(x, groups)
+    _check_like("dy", dy, x.dtype, x.numel(), x.shape)
+    _check_like("gamma", gamma, x.dtype, c)
+    _check_like("mean", mean, torch.float32, n * groups)
+    _check_like("rstd", rstd, torch.float32, n * groups)
+    _check_like("dx", dx, x.dtype, x.numel(), x.shape)
+    _check_like("dgamma", dgamma, torch.float32, c)
+    _check_like("dbeta", dbeta if with_dbeta else None, torch.float32, c)
+    for name, t in (("x", x), ("dy", dy), ("gamma", gamma), ("mean", mean), ("rstd", rstd)):
+        _check_cuda(name, t, x.device)
     code = DTYPE_CODES[x.dtype]
     dx = torch.empty_like(x) if dx is None else dx
     dgamma = torch.empty(c, dtype=torch.float32, device=x.device) if dgamma is None else dgamma
@@ -500,6 +547,10 @@ def group_norm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mean:
     need = int(lib.group_norm_bwd_workspace_size(n, c, sp, int(groups), code))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    for name, t in (("dx", dx), ("dgamma", dgamma), ("workspace", workspace)):
+        _check_cuda(name, t, x.device)
+    if with_dbeta:
+        _check_cuda("dbeta", dbeta, x.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(x.device):
         st = lib.group_norm_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(mean), _ptr(rstd), _ptr(dx),

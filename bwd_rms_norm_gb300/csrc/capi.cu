@@ -34,11 +34,14 @@ int elem_bytes(int dtype) { return dtype == RMSN_F32 ? 4 : 2; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
 int cuda_fail(cudaError_t e) {
   t_last_cuda_error = (int)e;
   return RMSN_ERR_CUDA;
 }
-}  // namespace
+
+void set_last_launches(int n) { t_last_launches = n; }
 
 LaunchLog& launch_log() { return t_launch_log; }
 

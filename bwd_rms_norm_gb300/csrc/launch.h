@@ -66,6 +66,12 @@ struct LaunchLog {
 LaunchLog& launch_log();
 // Start of a C-ABI call on this thread: clears the launch count and log.
 void begin_call();
+// Record a failed CUDA call for rms_norm_last_cuda_error(); returns
+// RMSN_ERR_CUDA.
+int cuda_fail(cudaError_t e);
+// Record how many kernels the current call enqueued, for
+// rms_norm_last_launch_count().
+void set_last_launches(int n);
 
 // Launch `kern` with programmatic dependent launch allowed (see pdl_wait in
 // common.cuh) and, when `cluster` > 1, thread-block clusters of `cluster`

@@ -59,18 +59,19 @@ extern "C" int rms_norm_bwd_noalloc(const void* dy, const void* x, const void* g
   if (!dw) return RMSN_ERR_NULL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (rows == 0) {
-    return cudaMemsetAsync(dw, 0, (size_t)hidden * sizeof(float), st) == cudaSuccess
-               ? RMSN_OK
-               : RMSN_ERR_CUDA;
+    const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)hidden * sizeof(float), st);
+    return e == cudaSuccess ? RMSN_OK : cuda_fail(e);
   }
   if (!dy || !x || !gamma || !rstd || !dx) return RMSN_ERR_NULL;
   const size_t need = rms_norm_bwd_workspace_size(rows, hidden, dtype);
   if (need > (size_t)RMSN_NOALLOC_SCRATCH_BYTES) return RMSN_ERR_SHAPE;
 
   int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess) return RMSN_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e);
   void* scratch = nullptr;
-  if (scratch_address(device, &scratch) != cudaSuccess) return RMSN_ERR_CUDA;
+  e = scratch_address(device, &scratch);
+  if (e != cudaSuccess) return cuda_fail(e);
 
   const int s = dtype == RMSN_F32 ? 4 : 2;
   auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
@@ -91,5 +92,8 @@ extern "C" int rms_norm_bwd_noalloc(const void* dy, const void* x, const void* g
   // rms_norm_bwd_workspace_size bytes
   a.max_partials = (int64_t)(need / ((size_t)hidden * sizeof(float)));
   int launches = 0;
-  return launch_bwd(dtype, a, st, &launches) == cudaSuccess ? RMSN_OK : RMSN_ERR_CUDA;
+  e = launch_bwd(dtype, a, st, &launches);
+  if (e != cudaSuccess) return cuda_fail(e);
+  set_last_launches(launches);
+  return RMSN_OK;
 }
