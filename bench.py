@@ -57,7 +57,7 @@ METRIC_GN = "GroupNorm fwd+bwd achieved HBM GB/s and % of GB300 peak; µs per ca
 
 def metric_for(w) -> str:
     return {"ln": METRIC_LN, "softmax": METRIC_SM, "gn": METRIC_GN}.get(w.kind, METRIC)
-DEFAULT_WORKLOAD = "llama_bf16_4096x4096"
+DEFAULT_WORKLOAD = "large_bf16_16384x8192_once"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -171,6 +171,77 @@ def summarize_clocks(lines, window):
     }
 
 
+class NvmlPoller:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, read-only queries) by a background thread about every
+    0.2 ms, so that even a timed region of a few milliseconds holds
+    samples.  ``window(t0, t1)`` summarises the samples taken between two
+    time.perf_counter() readings.  Inactive (no samples) when NVML cannot be
+    loaded."""
+
+    # clock-event reason bits of nvml.h
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        import threading
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                return
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            return
+        self._nv, self._h, self._reasons_fn = nv, h, reasons_fn
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def _run(self):
+        import ctypes
+        mhz, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            if self._nv.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(mhz)) == 0:
+                ok = self._reasons_fn(self._h, ctypes.byref(rs)) == 0
+                self.samples.append((t, mhz.value, rs.value if ok else 0))
+            time.sleep(0.0002)
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def window(self, t0: float, t1: float):
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        if not inside:
+            return None
+        bits = 0
+        for x in inside:
+            bits |= x[2]
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "reasons": sorted(v for k, v in self.REASONS.items() if bits & k),
+                "samples": len(inside)}
+
+
+def paired_variant(name: str):
+    """The other cast mode of a workload that exists in both (timed in the
+    same run as the requested one), or None."""
+    import workloads as W
+    table = W.all_workloads()
+    for a, b in (("_once", "_twice"), ("_twice", "_once")):
+        if name.endswith(a) and name[:-len(a)] + b in table:
+            return name[:-len(a)] + b
+    return None
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -202,15 +273,18 @@ def workload_by_name(name: str):
     return table[name]
 
 
-def time_oracle(w, rows: int):
+def time_oracle(w, rows: int, threads: int = 1):
     """Seconds for one oracle forward + backward over ``rows`` rows of ``w``
-    (inputs drawn once per row count, outside the timing)."""
+    (inputs drawn once per row count, outside the timing), the rows split
+    into ``threads`` contiguous ranges run on as many host threads; the
+    per-range parameter gradients are summed in range order."""
     import workloads as W
     from oracle import fp8 as of8
     from oracle import group_norm as ogn
     from oracle import layer_norm as oln
     from oracle import rms_norm as orm
     from oracle import softmax as osm
+    from oracle import threads as OT
     ws = w.with_(rows=rows)
     if (ws.name, rows) not in _ORACLE_INPUTS:
         _ORACLE_INPUTS.clear()
@@ -218,23 +292,65 @@ def time_oracle(w, rows: int):
         _ORACLE_INPUTS[(ws.name, rows)] = tuple(
             W.as_float64(inp[k]) if k in inp else None for k in ("x", "gamma", "dy", "beta"))
     xd, gd, dyd, bd = _ORACLE_INPUTS[(ws.name, rows)]
+
+    def run(sl):
+        xs, dys = xd[sl], dyd[sl]
+        if ws.kind == "softmax":
+            y = osm.forward(xs, ws.dtype)
+            osm.backward(dys, y, ws.dtype)
+            return None
+        if ws.kind == "gn":
+            _, mean, rstd = ogn.forward(xs, gd, bd, ws.groups, ws.eps, ws.dtype)
+            return ogn.backward(dys, xs, gd, mean, rstd, ws.groups, ws.dtype)[1]
+        if ws.kind == "ln":
+            _, mean, rstd = oln.forward(xs, gd, bd, ws.eps, ws.dtype)
+            return oln.backward(dys, xs, gd, mean, rstd, ws.dtype)[1]
+        if ws.out_fmt == "e4m3":
+            _, rstd = of8.forward_fp8(xs, gd, ws.eps, ws.offset, ws.scale)
+        else:
+            _, rstd = orm.forward(xs, gd, ws.eps, ws.offset, ws.dtype, ws.cast_mode)
+        return orm.backward(dys, xs, gd, rstd, ws.offset, ws.dtype)[1]
+
     t = time.perf_counter()
-    if ws.kind == "softmax":
-        y = osm.forward(xd, ws.dtype)
-        osm.backward(dyd, y, ws.dtype)
-    elif ws.kind == "gn":
-        _, mean, rstd = ogn.forward(xd, gd, bd, ws.groups, ws.eps, ws.dtype)
-        ogn.backward(dyd, xd, gd, mean, rstd, ws.groups, ws.dtype)
-    elif ws.kind == "ln":
-        _, mean, rstd = oln.forward(xd, gd, bd, ws.eps, ws.dtype)
-        oln.backward(dyd, xd, gd, mean, rstd, ws.dtype)
-    elif ws.out_fmt == "e4m3":
-        _, rstd = of8.forward_fp8(xd, gd, ws.eps, ws.offset, ws.scale)
-        orm.backward(dyd, xd, gd, rstd, ws.offset, ws.dtype)
-    else:
-        _, rstd = orm.forward(xd, gd, ws.eps, ws.offset, ws.dtype, ws.cast_mode)
-        orm.backward(dyd, xd, gd, rstd, ws.offset, ws.dtype)
+    parts = OT.map_rows(run, rows, threads)
+    if parts[0] is not None:
+        OT.sum_in_order(parts)
     return time.perf_counter() - t, ws.step_bytes()
+
+
+def host_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_baseline(w, name: str, budget_s: float = 10.0):
+    """The float64 oracle timed on the host on a bounded sample of the
+    workload (its first rows, about 16 M elements, a different seeded draw
+    of the same distributions): passes on one thread, then on every host
+    core, each repeated until about ``budget_s`` seconds of host time (at
+    least one pass).  GB/s of the sample's algorithmic bytes."""
+    rows = min(w.rows, max(16, (1 << 24) // max(1, w.hidden)))
+    out = {}
+    for threads in sorted({1, host_threads()}):
+        secs, nbytes, passes = 0.0, 0, 0
+        while (secs < budget_s and passes < 50) or passes == 0:
+            s_, b_ = time_oracle(w, rows, threads)
+            secs += s_
+            nbytes += b_
+            passes += 1
+        out[threads] = (nbytes / secs / 1e9, passes, secs)
+    cores = max(out)
+    v1, p1, s1 = out[1]
+    vn, pn, sn = out[cores]
+    return {"value": round(vn, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{name}: float64 forward+backward (numpy) over {rows} of {w.rows} rows "
+                       f"per pass: {pn} passes on {cores} threads, the rows split in {cores} "
+                       f"contiguous ranges ({sn:.1f} s); {p1} passes on 1 thread ({s1:.1f} s)"),
+            "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1},
+            "nproc": os.cpu_count()}
 
 
 def run_ours(args, rank, world, local):
@@ -367,7 +483,9 @@ def run_ours(args, rank, world, local):
     bwd_us = min(timed(g_bwd, 4) for _ in range(3)) * 1e3 / (4 * reps)
 
     uuid = str(getattr(props, "uuid", "")) or str(local)
-    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.isdigit() else uuid)
+    gpu_id = ("GPU-" + uuid) if uuid and not uuid.isdigit() else uuid
+    sampler = ClockSampler(gpu_id)
+    poller = NvmlPoller(gpu_id)
     t_soak = time.time()
     while time.time() - t_soak < 0.6:      # clocks settle on the same work
         g_fwd.replay()
@@ -383,10 +501,12 @@ def run_ours(args, rank, world, local):
     g_steps.replay()
     e1.record(stream)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
+    wall1 = time.perf_counter()
+    wall = wall1 - wall0
     barrier(world)
     t_end = time.time()
     sampler.mark(t_start, t_end)
+    in_region = poller.window(wall0, wall1)
     step_ms = e0.elapsed_time(e1)
     step_ms = reduce_max(step_ms, world, dev)
     # keep sampling a little after the timed region so that short regions
@@ -396,12 +516,68 @@ def run_ours(args, rank, world, local):
         g_steps.replay()
         torch.cuda.synchronize()
     clocks = sampler.stop()
+    poller.stop()
+    if in_region is not None:
+        # NVML samples taken inside the timed replay decide the clock and the
+        # reasons; nvidia-smi's (around it) stay beside them
+        clocks = {"sm_mhz": in_region["sm_mhz"], "sm_max_mhz": clocks.get("sm_max_mhz"),
+                  "reasons": sorted(set(in_region["reasons"]) | set(clocks.get("reasons", []))),
+                  "samples_in_timed_region": in_region["samples"],
+                  "source": "NVML polled about every 0.2 ms inside the timed replay; "
+                            "nvidia-smi every 50 ms around it",
+                  "nvidia_smi": clocks}
 
     ms_per_step = step_ms / args.steps
     total_bytes = w.step_bytes() * args.steps * world
     value = total_bytes / (step_ms * 1e-3) / 1e9
 
     peak, peak_src = measured_peak_gbs()
+
+    # The same workload with the other cast mode, on the same device buffers
+    # (same seeded inputs): its own step graph and forward graph.  The cast
+    # mode does not enter the backward, which is the one timed above.
+    variants = []
+    vname = None
+    if not (args.no_variant or ln or sm or gn or f8):
+        vname = paired_variant(args.workload)
+    if vname is not None:
+        wv = workload_by_name(vname)
+        if args.rows:
+            wv = wv.with_(rows=args.rows)
+
+        def fwd_v(k):
+            S = sets[k]
+            L.rms_norm_fwd(S["x"], g, wv.eps, wv.offset, wv.cast_mode, y=S["y"], rstd=S["rstd"])
+
+        def step_v(i):
+            fwd_v(i % nsets)
+            bwd((i + half) % nsets)
+
+        for i in range(nsets):
+            step_v(i)
+        torch.cuda.synchronize()
+        gv_steps = capture(step_v, args.steps)
+        gv_fwd = capture(lambda i: fwd_v(i % nsets), reps)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            gv_fwd.replay()
+            g_bwd.replay()
+        fwd_us_v = min(timed(gv_fwd, 4) for _ in range(3)) * 1e3 / (4 * reps)
+        gv_steps.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_v = reduce_max(timed(gv_steps, 1), world, dev)
+        value_v = wv.step_bytes() * args.steps * world / (ms_v * 1e-3) / 1e9
+        fwd_ach_v = wv.fwd_bytes() / (fwd_us_v * 1e-6) / 1e9
+        variants.append({
+            "workload": vname, "cast_mode": wv.cast_mode, "value": round(value_v, 1),
+            "unit": "GB/s", "ms_per_step": round(ms_v / args.steps, 6),
+            "pct_of_hbm_peak": round(100.0 * value_v / world / peak, 2),
+            "fwd_us": round(fwd_us_v, 3), "roofline_fwd_frac": round(fwd_ach_v / peak, 4),
+            "bwd_us": round(bwd_us, 3),
+            "timing": ("one CUDA-graph replay of exactly `steps` steps of this cast mode, "
+                       "CUDA events; the backward is the same call as the headline's"),
+        })
     fwd_ach = w.fwd_bytes() / (fwd_us * 1e-6) / 1e9
     bwd_ach = w.bwd_bytes() / (bwd_us * 1e-6) / 1e9
     traffic = load_traffic(args.workload)
@@ -413,18 +589,7 @@ def run_ours(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        # whole-workload passes of the oracle, repeated until about 10 s of
-        # host time have been spent
-        secs, nbytes, passes = 0.0, 0, 0
-        while secs < 10.0 and passes < 50:
-            s_, b_ = time_oracle(w, w.rows)
-            secs += s_
-            nbytes += b_
-            passes += 1
-        cpu = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1,
-               "kind": "oracle",
-               "sample": f"{args.workload}: {passes} float64 forward+backward passes over all "
-                         f"{w.rows} rows ({secs:.1f} s, numpy, single thread)"}
+        cpu = oracle_baseline(w, args.workload)
 
     op = "layer_norm" if ln else "softmax" if sm else "group_norm" if gn else "rms_norm"
     fwd_name = f"{op}_fwd" + ("_fp8" if f8 else "")
@@ -479,6 +644,7 @@ def run_ours(args, rank, world, local):
         },
         "isolated_call": iso,
         "e2e": e2e,
+        "variants": variants,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
@@ -618,7 +784,7 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
                 h.copy_(t.view(-1), non_blocking=True)
             drained[k].record(s_out)
 
-    for i in range(4):
+    for i in range(10):
         one(i)
     torch.cuda.synchronize()
     t = time.perf_counter()
@@ -628,11 +794,56 @@ def run_e2e(L, w, inp, dev, steps: int, with_beta: bool = False):
     secs = (time.perf_counter() - t) / steps
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in [hy, hdx] + hstats + hgrads)
+
+    # the host link alone, on the same pinned buffers and streams: the bound
+    # of the figure above
+    def copies(up: bool, down: bool, reps: int = 5):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            d = sets[0]
+            if up:
+                with torch.cuda.stream(s_in):
+                    for name, v in host_in.items():
+                        d[name].copy_(v, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s_out):
+                    hy.copy_(d["y"].view(torch.uint8) if f8 else d["y"], non_blocking=True)
+                    hdx.copy_(d["dx"], non_blocking=True)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    t_up, t_down, t_both = copies(True, False), copies(False, True), copies(True, True)
+    big_d2h = hy.numel() * hy.element_size() + hdx.numel() * hdx.element_size()
     return {"value": round(w.step_bytes() / secs / 1e9, 2), "unit": "GB/s",
             "us_per_step": round(secs * 1e6, 2),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "timing": ("wall clock over steps, synchronised at both ends; copies in, kernels "
-                       "and copies out on three streams over two device buffer sets")}
+            "timing": ("wall clock over steps after 10 warm-up steps, synchronised at both "
+                       "ends; copies in, kernels and copies out on three streams over two "
+                       "device buffer sets; host buffers pinned once before the warm-up"),
+            "host_link_gbs": {"h2d": round(h2d / t_up / 1e9, 1),
+                              "d2h": round(big_d2h / t_down / 1e9, 1),
+                              "both_directions": round((h2d + big_d2h) / t_both / 1e9, 1)},
+            "numa": numa_placement(dev)}
+
+
+def numa_placement(dev):
+    """NUMA node of the GPU (from its PCI device) and the host's node count;
+    pinned host buffers are first-touched by this process on its cores."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    out = {"host_nodes": len([d for d in os.listdir("/sys/devices/system/node")
+                              if d.startswith("node") and d[4:].isdigit()])
+           if os.path.isdir("/sys/devices/system/node") else None,
+           "cpus_allowed": host_threads()}
+    try:
+        bus = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            out["gpu_node"] = int(f.read().strip())
+        out["gpu_pci"] = bus
+    except (AttributeError, OSError, ValueError):
+        out["gpu_node"] = None
+    return out
 
 
 def code_of(text: str) -> str:
@@ -681,23 +892,25 @@ def run_reference(args, rank, world, local):
     if rank != 0:
         return
     w = workload_by_name(args.workload)
+    threads = host_threads()
     # size the sample so that warmup + steps take about two minutes
-    nprobe = max(1, min(64, (1 << 22) // w.hidden))
-    probe, _ = time_oracle(w, nprobe)
+    nprobe = max(threads, min(64 * threads, (1 << 22) // w.hidden))
+    probe, _ = time_oracle(w, nprobe, threads)
     per_row = probe / nprobe
     budget = 120.0 / max(1, args.steps + args.warmup)
     rows = int(max(min(16, w.rows), min(w.rows, budget / per_row)))
     for _ in range(args.warmup):
-        time_oracle(w, rows)
+        time_oracle(w, rows, threads)
     times = []
     nbytes = 0
     for _ in range(args.steps):
-        s, nbytes = time_oracle(w, rows)
+        s, nbytes = time_oracle(w, rows, threads)
         times.append(s)
     total = sum(times)
     value = nbytes * len(times) / total / 1e9
     sample = (f"{args.workload}: float64 oracle forward+backward over {rows} of {w.rows} rows "
-              f"per step (numpy, single thread)")
+              f"per step (numpy), the rows split in {threads} contiguous ranges on {threads} "
+              f"host threads")
     line = {
         "impl": "reference",
         "metric": metric_for(w),
@@ -714,8 +927,8 @@ def run_reference(args, rank, world, local):
         "data": "synthetic (seeded, see workloads/)",
         "config": {"workload": args.workload, "rows": w.rows, "hidden": w.hidden,
                    "sample_rows": rows},
-        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1,
-                         "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample, "nproc": os.cpu_count()},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -733,6 +946,8 @@ def main(argv=None):
                     help="override the workload's row count (profiling a larger case)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variant", action="store_true",
+                    help="skip timing the other cast mode of a workload that has both")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

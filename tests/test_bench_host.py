@@ -114,3 +114,50 @@ def test_fewer_than_three_warmup_steps_are_refused():
     with pytest.raises(SystemExit):
         with contextlib.redirect_stderr(io.StringIO()):
             bench.main(["--warmup", "2"])
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    """The headline line runs 16384 x 8192 bf16 (round once), the largest
+    configuration, and times the round-twice store in the same run."""
+    assert bench.DEFAULT_WORKLOAD == "large_bf16_16384x8192_once"
+    sizes = {n: w.step_bytes() for n, w in W.all_workloads().items()}
+    assert sizes[bench.DEFAULT_WORKLOAD] >= max(sizes.values()) - 200_000
+    assert bench.paired_variant(bench.DEFAULT_WORKLOAD) == "large_bf16_16384x8192_twice"
+    assert bench.paired_variant("large_bf16_16384x8192_twice") == "large_bf16_16384x8192_once"
+    assert bench.paired_variant("llama_bf16_4096x4096") is None
+
+
+def test_threaded_oracle_matches_one_thread():
+    """The all-core oracle baseline runs the unchanged oracle on contiguous
+    row ranges: y and dx are those of one pass over all rows, and the weight
+    gradient is the per-range sums added in range order."""
+    import numpy as np
+    from oracle import rms_norm as orm
+    from oracle import threads as OT
+    w = W.LLAMA_BF16_4096x4096.with_(rows=37, hidden=256)
+    inp = W.make_inputs(w)
+    xd, gd, dyd = (W.as_float64(inp[k]) for k in ("x", "gamma", "dy"))
+    y1, r1 = orm.forward(xd, gd, w.eps, 0, "bf16")
+    dx1, dw1 = orm.backward_exact(dyd, xd, gd, r1, 0)
+
+    def run(sl):
+        y, r = orm.forward(xd[sl], gd, w.eps, 0, "bf16")
+        dx, dw = orm.backward_exact(dyd[sl], xd[sl], gd, r, 0)
+        return y, dx, dw
+
+    parts = OT.map_rows(run, w.rows, 4)
+    assert [len(r) for r in OT.row_ranges(37, 4)] == [9, 9, 9, 10]
+    assert np.array_equal(np.concatenate([p[0] for p in parts]), y1)
+    assert np.array_equal(np.concatenate([p[1] for p in parts]), dx1)
+    dw = OT.sum_in_order([p[2] for p in parts])
+    np.testing.assert_allclose(dw, dw1, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(dw, ((parts[0][2] + parts[1][2]) + parts[2][2]) + parts[3][2])
+
+
+def test_oracle_baseline_reports_both_core_counts(monkeypatch):
+    monkeypatch.setattr(bench, "host_threads", lambda: 3)
+    w = W.FP32_256x1024.with_(rows=64, hidden=128)
+    cpu = bench.oracle_baseline(w, "tiny", budget_s=0.05)
+    assert cpu["kind"] == "oracle" and cpu["cores"] == 3
+    assert cpu["single_thread"]["cores"] == 1 and cpu["single_thread"]["value"] > 0
+    assert cpu["value"] > 0 and "3 threads" in cpu["sample"]
