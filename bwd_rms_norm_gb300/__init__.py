@@ -14,6 +14,13 @@ The functions carry the names of the C entry points declared in
 * ``rms_norm_bwd_workspace_size(rows, hidden, dtype)``
 * ``rms_norm_status_string(status)``
 * ``rms_norm_bwd_noalloc(dy, x, gamma, rstd, offset=0)`` -> ``(dx, dw)``
+* ``rms_norm_bwd_blocked(dy, x, gamma, rstd, block_rows, offset=0)`` ->
+  ``(dx, chunk_sums)``; ``rms_norm_dw_sum(chunk_sums)`` -> ``dw``;
+  ``rms_norm_dw_chunk_count(rows, block_rows)``;
+  ``rms_norm_bwd_blocked_workspace_size(rows, hidden, block_rows)``;
+  ``rms_norm_rank_rows(rows, block_rows, world, rank)`` -> ``(lo, hi)`` (the
+  weight gradient in an order that any split of the rows reproduces)
+* ``rms_norm_set_sm_budget(sms)``, ``rms_norm_sm_budget()
 * ``rms_norm_fwd_fp8(x, gamma, scale, eps, offset=0)`` -> ``(y8, rstd)``
   (``y8`` a torch.float8_e4m3fn tensor, ``scale`` a one-element fp32
   device tensor)
@@ -46,6 +53,7 @@ RMSN_ROUND_ONCE, RMSN_ROUND_TWICE = 0, 1
 RMSN_OK = 0
 RMSN_MAX_HIDDEN = 65536
 RMSN_MAX_PARTIALS = 1024
+RMSN_DW_CHUNK_BLOCKS = 32
 
 DTYPE_CODES = {torch.float32: RMSN_F32, torch.bfloat16: RMSN_BF16, torch.float16: RMSN_F16}
 CAST_MODES = {"round_once": RMSN_ROUND_ONCE, "round_twice": RMSN_ROUND_TWICE}
@@ -59,6 +67,13 @@ EXPORTED = (
     "rms_norm_last_launch_count",
     "rms_norm_last_kernels",
     "rms_norm_bwd_noalloc",
+    "rms_norm_bwd_blocked_workspace_size",
+    "rms_norm_dw_chunk_count",
+    "rms_norm_bwd_blocked",
+    "rms_norm_dw_sum",
+    "rms_norm_rank_rows",
+    "rms_norm_set_sm_budget",
+    "rms_norm_sm_budget",
     "rms_norm_wait_timeouts",
     "rms_norm_fwd_fp8",
     "layer_norm_fwd",
@@ -109,6 +124,20 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_last_launch_count.restype = I
     lib.rms_norm_bwd_noalloc.argtypes = [P, P, P, P, P, P, I64, I64, I, I, P]
     lib.rms_norm_bwd_noalloc.restype = I
+    lib.rms_norm_bwd_blocked_workspace_size.argtypes = [I64, I64, I64]
+    lib.rms_norm_bwd_blocked_workspace_size.restype = SZ
+    lib.rms_norm_dw_chunk_count.argtypes = [I64, I64]
+    lib.rms_norm_dw_chunk_count.restype = I64
+    lib.rms_norm_bwd_blocked.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, P, SZ, P]
+    lib.rms_norm_bwd_blocked.restype = I
+    lib.rms_norm_dw_sum.argtypes = [P, I64, I64, P, P]
+    lib.rms_norm_dw_sum.restype = I
+    lib.rms_norm_rank_rows.argtypes = [I64, I64, I, I, ctypes.POINTER(I64), ctypes.POINTER(I64)]
+    lib.rms_norm_rank_rows.restype = I
+    lib.rms_norm_set_sm_budget.argtypes = [I]
+    lib.rms_norm_set_sm_budget.restype = I
+    lib.rms_norm_sm_budget.argtypes = []
+    lib.rms_norm_sm_budget.restype = I
     lib.rms_norm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.rms_norm_wait_timeouts.restype = I
     lib.rms_norm_fwd_fp8.argtypes = [P, P, P, P, P, I64, I64, F, I, I, P]
@@ -349,6 +378,102 @@ def rms_norm_bwd_noalloc(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor,
     if st != RMSN_OK:
         raise RMSNormError("rms_norm_bwd_noalloc", st)
     return dx, dw
+
+
+def rms_norm_dw_chunk_count(rows: int, block_rows: int) -> int:
+    """Chunk sums ``rms_norm_bwd_blocked`` writes for ``rows`` rows."""
+    n = int(load_library().rms_norm_dw_chunk_count(int(rows), int(block_rows)))
+    if n < 0:
+        raise RMSNormError("rms_norm_dw_chunk_count", -n)
+    return n
+
+
+def rms_norm_bwd_blocked_workspace_size(rows: int, hidden: int, block_rows: int) -> int:
+    """Bytes of workspace ``rms_norm_bwd_blocked`` needs."""
+    return int(load_library().rms_norm_bwd_blocked_workspace_size(int(rows), int(hidden),
+                                                                  int(block_rows)))
+
+
+def rms_norm_rank_rows(rows: int, block_rows: int, world: int, rank: int) -> Tuple[int, int]:
+    """Rank ``rank``'s slab [lo, hi) of ``rows`` rows in whole chunks of
+    ``RMSN_DW_CHUNK_BLOCKS * block_rows`` rows (no device needed)."""
+    lo, hi = ctypes.c_int64(0), ctypes.c_int64(0)
+    st = load_library().rms_norm_rank_rows(int(rows), int(block_rows), int(world), int(rank),
+                                           ctypes.byref(lo), ctypes.byref(hi))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_rank_rows", st)
+    return int(lo.value), int(hi.value)
+
+
+def rms_norm_bwd_blocked(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor,
+                         rstd: torch.Tensor, block_rows: int, offset: int = 0,
+                         dx: Optional[torch.Tensor] = None,
+                         chunk_sums: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None):
+    """Backward with the weight gradient left as chunk sums over fixed blocks
+    of ``block_rows`` rows; returns ``(dx, chunk_sums)``, ``chunk_sums`` fp32
+    of shape [rms_norm_dw_chunk_count(rows, block_rows), hidden].  Adding
+    them with ``rms_norm_dw_sum`` gives the same dw for any split of the rows
+    into whole chunks (see ``rms_norm_rank_rows``)."""
+    lib = load_library()
+    rows, hidden = _check_bwd_args(dy, x, gamma, rstd, dx, None)
+    if int(block_rows) < 1:
+        raise RuntimeError("block_rows must be at least 1")
+    nchunks = rms_norm_dw_chunk_count(rows, block_rows)
+    _check_like("chunk_sums", chunk_sums, torch.float32, nchunks * hidden)
+    for name, t in (("x", x), ("dy", dy), ("gamma", gamma), ("rstd", rstd)):
+        _check_cuda(name, t, x.device)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if chunk_sums is None:
+        chunk_sums = torch.empty(nchunks, hidden, dtype=torch.float32, device=x.device)
+    need = rms_norm_bwd_blocked_workspace_size(rows, hidden, block_rows)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    for name, t in (("dx", dx), ("chunk_sums", chunk_sums), ("workspace", workspace)):
+        _check_cuda(name, t, x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(x.device):
+        st = lib.rms_norm_bwd_blocked(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx),
+                                      _ptr(chunk_sums), rows, hidden, int(block_rows),
+                                      int(offset), DTYPE_CODES[x.dtype], workspace.data_ptr(),
+                                      ws_bytes, _stream_handle(x.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_bwd_blocked", st)
+    return dx, chunk_sums
+
+
+def rms_norm_dw_sum(chunk_sums: torch.Tensor, dw: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """dw [hidden] = the chunk sums [nchunks, hidden] added in chunk order."""
+    lib = load_library()
+    if chunk_sums.dim() != 2 or chunk_sums.dtype != torch.float32:
+        raise RuntimeError("chunk_sums must be a float32 [nchunks, hidden] tensor")
+    nchunks, hidden = chunk_sums.shape
+    _check_like("dw", dw, torch.float32, hidden)
+    _check_cuda("chunk_sums", chunk_sums)
+    if dw is None:
+        dw = torch.empty(hidden, dtype=torch.float32, device=chunk_sums.device)
+    _check_cuda("dw", dw, chunk_sums.device)
+    with torch.cuda.device(chunk_sums.device):
+        st = lib.rms_norm_dw_sum(_ptr(chunk_sums), nchunks, hidden, _ptr(dw),
+                                 _stream_handle(chunk_sums.device, stream))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_dw_sum", st)
+    return dw
+
+
+def rms_norm_set_sm_budget(sms: int) -> None:
+    """Let the persistent kernels use at most ``sms`` SMs' worth of
+    resident CTAs (0: every SM); process-wide, read at each launch."""
+    st = load_library().rms_norm_set_sm_budget(int(sms))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_set_sm_budget", st)
+
+
+def rms_norm_sm_budget() -> int:
+    return int(load_library().rms_norm_sm_budget())
 
 
 def layer_norm_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Tensor], eps: float,

@@ -9,17 +9,21 @@
 // backward formula; the one above is the exact derivative of the forward.
 //
 // Structure (two launches on one stream, no host synchronisation):
-//   1. a persistent row kernel.  CTA b of G owns the contiguous rows
-//      [b*R/G, (b+1)*R/G).  Each thread owns a fixed set of columns, keeps
-//      their gains and their fp32 dw accumulators in registers for all of
-//      the CTA's rows, and at the end writes them as partial row b of the
+//   1. a persistent row kernel.  The rows are cut into blocks (RowBlocks in
+//      common.cuh): one per CTA, the rows split evenly, for rms_norm_bwd;
+//      `brows` rows each, whole blocks dealt to the CTAs, for the
+//      fixed-block backward.  Each thread owns a fixed set of columns, keeps
+//      their gains and their fp32 dw accumulators in registers, and at the
+//      end of every block writes them as that block's partial row of the
 //      workspace.  The next row's x, dy and rstd are loaded while the
 //      current row is reduced.
-//   2. dw_finalize: dw[j] = sum over b of partial[b][j] in a fixed order,
-//      launched as a programmatic dependent launch so that its launch
-//      overlaps the tail of kernel 1.
-// Because G depends only on the sizes and the GPU's SM count and every sum
-// has a fixed order, repeated calls give bit-identical dw.
+//   2. dw_finalize (or, for the fixed-block backward, dw_chunk_sums): the
+//      partial rows added in a fixed order, launched as a programmatic
+//      dependent launch so that its launch overlaps the tail of kernel 1.
+// A block's partial depends only on its rows, and every sum has a fixed
+// order: repeated calls are bit-identical, and the fixed-block backward's
+// chunk sums do not change when the same rows are split over more or fewer
+// CTAs, or over several calls along whole chunks.
 #include "common.cuh"
 #include "launch.h"
 
@@ -59,7 +63,7 @@ template <typename T, int VPT, bool PREFETCH>
 __global__ void __launch_bounds__(1024) bwd_cta_rows(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
-    int64_t rows, int hidden, float off) {
+    int64_t rows, int hidden, float off, int brows) {
   constexpr int E = Traits<T>::kVec;
   __shared__ float red[64];
   // Let the finalize kernel be scheduled now; it waits for this grid to
@@ -67,8 +71,8 @@ __global__ void __launch_bounds__(1024) bwd_cta_rows(
   pdl_trigger();
   pdl_wait();
   const int nvec = hidden / E;
-  const int64_t r0 = (int64_t)blockIdx.x * rows / gridDim.x;
-  const int64_t r1 = (int64_t)(blockIdx.x + 1) * rows / gridDim.x;
+  const RowBlocks rw = row_blocks(rows, brows, blockIdx.x, gridDim.x);
+  const int64_t r0 = rw.r0, r1 = rw.r0 + rw.n;
   const float inv_n_div = (float)hidden;
 
   float ge[VPT][E];
@@ -90,7 +94,9 @@ __global__ void __launch_bounds__(1024) bwd_cta_rows(
   RowBuf<T, VPT> cur, nxt;
   if (PREFETCH && r0 < r1) load_row<T, VPT>(cur, dy, x, rstd, r0, hidden, nvec);
   int parity = 0;
-  for (int64_t r = r0; r < r1; ++r) {
+  int64_t part = rw.b0;
+  for (int64_t r = r0; r < r1; ++part) {
+   for (const int64_t end = r0 + rw.block_end((int)(r - r0)); r < end; ++r) {
     if (PREFETCH) {
       if (r + 1 < r1) load_row<T, VPT>(nxt, dy, x, rstd, r + 1, hidden, nvec);
     } else {
@@ -133,19 +139,8 @@ __global__ void __launch_bounds__(1024) bwd_cta_rows(
       }
     }
     if (PREFETCH) cur = nxt;
-  }
-
-  float* pr = partial + (int64_t)blockIdx.x * hidden;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = threadIdx.x + k * blockDim.x;
-    if (v < nvec) {
-#pragma unroll
-      for (int i = 0; i < E; i += 4) {
-        const float4 q = make_float4(acc[k][i], acc[k][i + 1], acc[k][i + 2], acc[k][i + 3]);
-        *reinterpret_cast<float4*>(pr + (int64_t)v * E + i) = q;
-      }
-    }
+   }
+    flush_partial<VPT, E>(acc, partial, part, hidden, 0, threadIdx.x, blockDim.x, nvec);
   }
 }
 
@@ -155,15 +150,17 @@ template <typename T>
 __global__ void __launch_bounds__(256) bwd_scalar(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
-    int64_t rows, int hidden, float off) {
+    int64_t rows, int hidden, float off, int brows) {
   __shared__ float red[64];
   pdl_trigger();
   pdl_wait();
-  const int64_t r0 = (int64_t)blockIdx.x * rows / gridDim.x;
-  const int64_t r1 = (int64_t)(blockIdx.x + 1) * rows / gridDim.x;
-  float* pr = partial + (int64_t)blockIdx.x * hidden;
+  const RowBlocks rw = row_blocks(rows, brows, blockIdx.x, gridDim.x);
+  const int64_t r0 = rw.r0, r1 = rw.r0 + rw.n;
   int parity = 0;
   for (int64_t r = r0; r < r1; ++r) {
+    // the block's partial row; its first row starts the sums
+    const int64_t in_block = (r - r0) % rw.brows;
+    float* pr = partial + (rw.b0 + (r - r0) / rw.brows) * (int64_t)hidden;
     const T* xr = x + r * hidden;
     const T* dr = dy + r * hidden;
     const float rs = rstd[r];
@@ -182,23 +179,32 @@ __global__ void __launch_bounds__(256) bwd_scalar(
       const float xh = Traits<T>::to_f(xr[j]) * rs;
       const float g = df * (Traits<T>::to_f(gamma[j]) + off);
       dxr[j] = Traits<T>::from_f(fmaf(-xh, c, g) * rs);
-      pr[j] = fmaf(df, xh, r == r0 ? 0.f : pr[j]);
+      pr[j] = fmaf(df, xh, in_block == 0 ? 0.f : pr[j]);
     }
   }
 }
 
-// out[j] = sum_b partial[b][j] over the `ncols` columns of a [nparts, ncols]
-// fp32 matrix, written to out0[j] for j < split and to out1[j - split]
-// otherwise.  Block (32 columns) x (kFinLanes lanes over b): lane t sums
-// b = t, t + kFinLanes, ... in increasing order, then lane 0 adds the lane
-// sums in order.  The order depends only on nparts.  Blocks of 512 threads
-// fit beside a resident CTA of the row kernel, so they are already waiting
-// when it finishes (programmatic dependent launch); measured on GB300, 8
-// lanes are slower (longer serial sums) and 32 no faster.
+// Two fixed summation orders of the partial rows [nparts, ncols].
+//
+// dw_finalize (every backward's own reduction): lane t of 16 adds rows t,
+// t + 16, t + 32, ... in increasing order, then lane 0 adds the 16 lane
+// sums in order.  The order depends only on nparts.  Blocks of 32 columns
+// x 16 lanes (512 threads): measured on GB300 behind the row kernels, this
+// shape -- loads in flight at once, one barrier, one short chain in shared
+// memory -- beat every form of a pairwise tree (per-thread trees of 32 loads,
+// trees across lanes through shared memory, warp-shuffle trees after a
+// transpose) by 1 to 3 us a call.
+//
+// dw_chunk_sums (the fixed-block backward): the rows form chunks of
+// kChunkParts = 32 consecutive rows (the last may be shorter); chunk c's sum
+// is ((s_0 + s_1) + ...) + s_15 with s_t = row 32c + t + row 32c + t + 16 (a
+// missing row counts as +0).  A chunk's sum depends on its 32 rows alone,
+// so a split of the rows into runs of whole chunks can form them
+// separately; dw_chunk_totals then adds chunk sums in chunk order.
 constexpr int kFinLanes = 16;
 
 __global__ void __launch_bounds__(32 * kFinLanes) dw_finalize(const float* __restrict__ partial,
-                                                             int nparts, int ncols,
+                                                             int64_t nparts, int ncols,
                                                              float* __restrict__ out0,
                                                              float* __restrict__ out1, int split) {
   pdl_trigger();
@@ -209,7 +215,7 @@ __global__ void __launch_bounds__(32 * kFinLanes) dw_finalize(const float* __res
   float a = 0.f;
   if (j < ncols) {
 #pragma unroll 8
-    for (int b = ty; b < nparts; b += kFinLanes) a += partial[(int64_t)b * ncols + j];
+    for (int64_t b = ty; b < nparts; b += kFinLanes) a += partial[b * ncols + j];
   }
   s[ty][tx] = a;
   __syncthreads();
@@ -224,36 +230,93 @@ __global__ void __launch_bounds__(32 * kFinLanes) dw_finalize(const float* __res
   }
 }
 
+// Chunk sums in passes of kPassChunks chunks: lane t forms s_t of every
+// chunk of the pass (its two loads per chunk all in flight at once), lanes
+// 0 .. nc-1 each add one chunk's 16 values in order, and the sums go to
+// chunks[c][j].
+constexpr int kPassChunks = 8;
+
+__global__ void __launch_bounds__(32 * kFinLanes) dw_chunk_sums(const float* __restrict__ partial,
+                                                               int64_t nparts, int ncols,
+                                                               float* __restrict__ chunks) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float s[kPassChunks][kFinLanes][33];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int j = blockIdx.x * 32 + tx;
+  const bool in = j < ncols;
+  const int64_t nchunks = (nparts + kChunkParts - 1) / kChunkParts;
+  for (int64_t g0 = 0; g0 < nchunks; g0 += kPassChunks) {
+    const int nc = (int)(nchunks - g0 < kPassChunks ? nchunks - g0 : kPassChunks);
+#pragma unroll
+    for (int c = 0; c < kPassChunks; ++c) {
+      const int64_t r = (g0 + c) * kChunkParts + ty;
+      const float lo = (c < nc && in && r < nparts) ? partial[r * ncols + j] : 0.f;
+      const float hi = (c < nc && in && r + kFinLanes < nparts)
+                           ? partial[(r + kFinLanes) * ncols + j] : 0.f;
+      s[c][ty][tx] = lo + hi;
+    }
+    __syncthreads();
+    if (ty < nc && in) {
+      float t = s[ty][0][tx];
+#pragma unroll
+      for (int l = 1; l < kFinLanes; ++l) t += s[ty][l][tx];
+      chunks[(g0 + ty) * ncols + j] = t;
+    }
+    __syncthreads();
+  }
+}
+
+// out[j] = chunks[0][j] + chunks[1][j] + ... in chunk order.
+__global__ void __launch_bounds__(256) dw_chunk_totals(const float* __restrict__ chunks,
+                                                       int64_t nchunks, int ncols,
+                                                       float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= ncols) return;
+  float t = chunks[j];
+#pragma unroll 8
+  for (int64_t c = 1; c < nchunks; ++c) t += chunks[c * ncols + j];
+  out[j] = t;
+}
+
 }  // namespace
 
-cudaError_t launch_column_sums(const float* partial, int nparts, int ncols, float* out0,
+cudaError_t launch_column_sums(const float* partial, int64_t nparts, int ncols, float* out0,
                                float* out1, int split, cudaStream_t s) {
-  return launch_kernel(dw_finalize, dim3((unsigned)((ncols + 31) / 32)), dim3(32, kFinLanes), 0, s, 1,
-                       partial, nparts, ncols, out0, out1, split);
+  return launch_kernel(dw_finalize, dim3((unsigned)((ncols + 31) / 32)), dim3(32, kFinLanes), 0,
+                       s, 1, partial, nparts, ncols, out0, out1, split);
+}
+
+cudaError_t launch_chunk_sums(const float* partial, int64_t nparts, int ncols, float* chunks,
+                              cudaStream_t s) {
+  return launch_kernel(dw_chunk_sums, dim3((unsigned)((ncols + 31) / 32)), dim3(32, kFinLanes),
+                       0, s, 1, partial, nparts, ncols, chunks);
+}
+
+cudaError_t launch_chunk_totals(const float* chunks, int64_t nchunks, int ncols, float* out,
+                                cudaStream_t s) {
+  return launch_kernel(dw_chunk_totals, dim3((unsigned)((ncols + 255) / 256)), dim3(256), 0, s,
+                       1, chunks, nchunks, ncols, out);
 }
 
 namespace {
 
-cudaError_t launch_finalize(const float* partial, float* dw, int nparts, int hidden,
-                            cudaStream_t s) {
-  return launch_column_sums(partial, nparts, hidden, dw, nullptr, hidden, s);
-}
-
 template <typename T, int VPT>
-cudaError_t launch_rows(const BwdArgs& a, int tpr, cudaStream_t s, int* nparts) {
+cudaError_t launch_rows(const BwdArgs& a, int tpr, cudaStream_t s, int64_t* nparts) {
   auto kern = bwd_cta_rows<T, VPT, VPT == 1>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const int occ = max_blocks_per_sm((const void*)kern, tpr, 0);
-  int64_t g = (int64_t)sm_count(dev) * (occ > 0 ? occ : 1);
-  if (g > a.rows) g = a.rows;
-  if (g > a.max_partials) g = a.max_partials;
-  *nparts = (int)g;
-  return launch_kernel(kern, dim3((unsigned)g), dim3(tpr), 0, s, 1,
+  const BlockPlan bp = plan_blocks(a.rows, a.block_rows,
+                                   unit_cap(a, (int64_t)sm_count(dev) * (occ > 0 ? occ : 1)));
+  *nparts = bp.nblocks;
+  return launch_kernel(kern, dim3((unsigned)bp.units), dim3(tpr), 0, s, 1,
                        static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
                        static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
-                       a.rows, a.hidden, a.offset ? 1.f : 0.f);
+                       a.rows, a.hidden, a.offset ? 1.f : 0.f, bp.brows);
 }
 
 template <typename T> int dtype_code();
@@ -266,7 +329,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s, int* launches) {
   constexpr int E = Traits<T>::kVec;
   const int nvec = a.hidden / E;
   const int max_vpt = E == 4 ? 4 : 2;  // at most 16 columns per thread
-  int nparts = 0;
+  int64_t nparts = 0;
   cudaError_t e = cudaErrorInvalidValue;
   // the staged pipeline where x and dy rows fit its ring, else the register
   // kernel, else (rows too wide for one CTA) a thread-block cluster, else the
@@ -290,18 +353,19 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t s, int* launches) {
     if (e != cudaSuccess) return e;
     auto kern = bwd_scalar<T>;
     const int occ = max_blocks_per_sm((const void*)kern, 256, 0);
-    int64_t g = (int64_t)sm_count(dev) * (occ > 0 ? occ : 1);
-    if (g > a.rows) g = a.rows;
-    if (g > a.max_partials) g = a.max_partials;
-    nparts = (int)g;
-    e = launch_kernel(kern, dim3((unsigned)g), dim3(256), 0, s, 1,
+    const BlockPlan bp = plan_blocks(a.rows, a.block_rows,
+                                     unit_cap(a, (int64_t)sm_count(dev) * (occ > 0 ? occ : 1)));
+    nparts = bp.nblocks;
+    e = launch_kernel(kern, dim3((unsigned)bp.units), dim3(256), 0, s, 1,
                       static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
                       static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
-                      a.rows, a.hidden, a.offset ? 1.f : 0.f);
+                      a.rows, a.hidden, a.offset ? 1.f : 0.f, bp.brows);
   }
   if (e != cudaSuccess) return e;
   *launches += 1;
-  e = launch_finalize(a.partial, a.dw, nparts, a.hidden, s);
+  e = a.chunks != nullptr ? launch_chunk_sums(a.partial, nparts, a.hidden, a.chunks, s)
+                          : launch_column_sums(a.partial, nparts, a.hidden, a.dw, nullptr,
+                                               a.hidden, s);
   if (e == cudaSuccess) *launches += 1;
   return e;
 }

@@ -18,6 +18,7 @@ thread_local LaunchLog t_launch_log = {{nullptr, nullptr, nullptr, nullptr}, 0};
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_sm_budget{0};  // 0: every SM
 
 struct OccEntry {
   const void* func;
@@ -52,15 +53,17 @@ void begin_call() {
 }
 
 int sm_count(int device) {
-  if (device >= 0 && device < kMaxDevices) {
-    int v = g_sm_count[device].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-  }
+  const int budget = g_sm_budget.load(std::memory_order_relaxed);
   int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0)
-    n = 1;
-  if (device >= 0 && device < kMaxDevices) g_sm_count[device].store(n, std::memory_order_relaxed);
-  return n;
+  if (device >= 0 && device < kMaxDevices) n = g_sm_count[device].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        n <= 0)
+      n = 1;
+    if (device >= 0 && device < kMaxDevices)
+      g_sm_count[device].store(n, std::memory_order_relaxed);
+  }
+  return budget > 0 && budget < n ? budget : n;
 }
 
 int max_blocks_per_sm(const void* func, int block, size_t smem) {
@@ -197,12 +200,108 @@ int rms_norm_bwd(const void* dy, const void* x, const void* gamma, const float* 
   a.partial = static_cast<float*>(workspace);
   a.max_partials = (int64_t)(workspace_bytes / ((size_t)hidden * sizeof(float)));
   if (a.max_partials > RMSN_MAX_PARTIALS) a.max_partials = RMSN_MAX_PARTIALS;
+  a.block_rows = 0;
+  a.chunks = nullptr;
   int launches = 0;
   cudaError_t e = launch_bwd(dtype, a, st, &launches);
   if (e != cudaSuccess) return cuda_fail(e);
   t_last_launches = launches;
   return RMSN_OK;
 }
+
+static int64_t blocks_of(int64_t rows, int64_t block_rows) {
+  return (rows + block_rows - 1) / block_rows;
+}
+
+size_t rms_norm_bwd_blocked_workspace_size(int64_t rows, int64_t hidden, int64_t block_rows) {
+  if (rows <= 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN ||
+      block_rows < 1)
+    return 0;
+  return (size_t)blocks_of(rows, block_rows) * (size_t)hidden * sizeof(float);
+}
+
+int64_t rms_norm_dw_chunk_count(int64_t rows, int64_t block_rows) {
+  if (rows < 0 || rows > RMSN_MAX_ROWS || block_rows < 1) return -RMSN_ERR_SHAPE;
+  return (blocks_of(rows, block_rows) + RMSN_DW_CHUNK_BLOCKS - 1) / RMSN_DW_CHUNK_BLOCKS;
+}
+
+int rms_norm_bwd_blocked(const void* dy, const void* x, const void* gamma, const float* rstd,
+                         void* dx, float* chunk_sums, int64_t rows, int64_t hidden,
+                         int64_t block_rows, int offset, int dtype, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (dtype != RMSN_F32 && dtype != RMSN_BF16 && dtype != RMSN_F16) return RMSN_ERR_DTYPE;
+  if (offset != 0 && offset != 1) return RMSN_ERR_ARG;
+  if (rows < 0 || rows > RMSN_MAX_ROWS || hidden < 1 || hidden > RMSN_MAX_HIDDEN)
+    return RMSN_ERR_SHAPE;
+  if (block_rows < 1 || block_rows > RMSN_MAX_ROWS) return RMSN_ERR_ARG;
+  begin_call();
+  if (rows == 0) return RMSN_OK;
+  if (!dy || !x || !gamma || !rstd || !dx || !chunk_sums || !workspace) return RMSN_ERR_NULL;
+  if (!aligned16(workspace)) return RMSN_ERR_ALIGN;
+  if (workspace_bytes < rms_norm_bwd_blocked_workspace_size(rows, hidden, block_rows))
+    return RMSN_ERR_WORKSPACE;
+  const int s = elem_bytes(dtype);
+  BwdArgs a;
+  a.dy = dy;
+  a.x = x;
+  a.gamma = gamma;
+  a.rstd = rstd;
+  a.dx = dx;
+  a.dw = nullptr;
+  a.rows = rows;
+  a.hidden = (int)hidden;
+  a.offset = offset;
+  a.vec_ok = ((hidden * s) % 16 == 0) && aligned16(dy) && aligned16(x) && aligned16(gamma) &&
+             aligned16(dx);
+  a.partial = static_cast<float*>(workspace);
+  a.max_partials = blocks_of(rows, block_rows);
+  a.block_rows = block_rows;
+  a.chunks = chunk_sums;
+  int launches = 0;
+  cudaError_t e = launch_bwd(dtype, a, static_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = launches;
+  return RMSN_OK;
+}
+
+int rms_norm_dw_sum(const float* chunk_sums, int64_t nchunks, int64_t hidden, float* dw,
+                    void* stream) {
+  if (nchunks < 0 || hidden < 1 || hidden > RMSN_MAX_HIDDEN) return RMSN_ERR_SHAPE;
+  begin_call();
+  if (!dw) return RMSN_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (nchunks == 0) {
+    const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)hidden * sizeof(float), st);
+    return e == cudaSuccess ? RMSN_OK : cuda_fail(e);
+  }
+  if (!chunk_sums) return RMSN_ERR_NULL;
+  const cudaError_t e = launch_chunk_totals(chunk_sums, nchunks, (int)hidden, dw, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  t_last_launches = 1;
+  return RMSN_OK;
+}
+
+int rms_norm_rank_rows(int64_t rows, int64_t block_rows, int world, int rank, int64_t* row_lo,
+                       int64_t* row_hi) {
+  if (!row_lo || !row_hi) return RMSN_ERR_NULL;
+  if (rows < 0 || rows > RMSN_MAX_ROWS) return RMSN_ERR_SHAPE;
+  if (block_rows < 1 || world < 1 || rank < 0 || rank >= world) return RMSN_ERR_ARG;
+  const int64_t chunk_rows = block_rows * RMSN_DW_CHUNK_BLOCKS;
+  const int64_t chunks = (rows + chunk_rows - 1) / chunk_rows;
+  const int64_t c0 = chunks * rank / world, c1 = chunks * (rank + 1) / world;
+  const int64_t lo = c0 * chunk_rows, hi = c1 * chunk_rows;
+  *row_lo = lo < rows ? lo : rows;
+  *row_hi = hi < rows ? hi : rows;
+  return RMSN_OK;
+}
+
+int rms_norm_set_sm_budget(int sms) {
+  if (sms < 0) return RMSN_ERR_ARG;
+  g_sm_budget.store(sms, std::memory_order_relaxed);
+  return RMSN_OK;
+}
+
+int rms_norm_sm_budget(void) { return g_sm_budget.load(std::memory_order_relaxed); }
 
 int layer_norm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
                    float* rstd, int64_t rows, int64_t hidden, float eps, int dtype,

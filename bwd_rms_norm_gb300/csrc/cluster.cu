@@ -62,7 +62,11 @@ __global__ void __launch_bounds__(512) fwd_cluster(
     for (int e = 0; e < E; ++e) ss = fmaf(f[e], f[e], ss);
   }
   ss = cluster_sum(ss, red, slots, 0, rank, csize);
-  const float rs = rstd_of(ss / (float)hidden, eps);
+  float rs = rstd_of(ss / (float)hidden, eps);
+  if (isinf(ss))  // the fp32 sum of squares overflowed (see kOverflowScale)
+    rs = rstd_rescaled(cluster_sum(scaled_sum_sq(xr + base * E, threadIdx.x, blockDim.x, nv * E),
+                                   red, slots, 1, rank, csize),
+                       hidden, eps);
   if (rank == 0 && threadIdx.x == 0) rstd[row] = rs;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
@@ -87,7 +91,7 @@ template <typename T, int VPT>
 __global__ void __launch_bounds__(512, 1) bwd_cluster(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
-    int64_t rows, int hidden, float off, int csize) {
+    int64_t rows, int hidden, float off, int csize, int brows) {
   constexpr int E = Traits<T>::kVec;
   __shared__ float red[64];
   __shared__ float slots[2 * kMaxCluster];
@@ -96,8 +100,8 @@ __global__ void __launch_bounds__(512, 1) bwd_cluster(
   const uint32_t rank = cta_rank();
   const int64_t cid = blockIdx.x / csize;
   const int64_t nclusters = gridDim.x / csize;
-  const int64_t r0 = cid * rows / nclusters;
-  const int64_t r1 = (cid + 1) * rows / nclusters;
+  const RowBlocks blk = row_blocks(rows, brows, cid, nclusters);
+  const int64_t r0 = blk.r0, r1 = blk.r0 + blk.n;
   const int nv = hidden / E / csize;
   const int64_t base = (int64_t)rank * nv;
 
@@ -128,7 +132,9 @@ __global__ void __launch_bounds__(512, 1) bwd_cluster(
   cluster_sync();  // every CTA of the cluster is running
   if (r0 < r1) load(r0, xc, dc, rc);
   int parity = 0;
-  for (int64_t r = r0; r < r1; ++r) {
+  int64_t part = blk.b0;
+  for (int64_t r = r0; r < r1; ++part) {
+   for (const int64_t end = r0 + blk.block_end((int)(r - r0)); r < end; ++r) {
     if (r + 1 < r1) load(r + 1, xn, dn, rn);
     float dot = 0.f;
 #pragma unroll
@@ -166,17 +172,8 @@ __global__ void __launch_bounds__(512, 1) bwd_cluster(
       dc[k] = dn[k];
     }
     rc = rn;
-  }
-  float* pr = partial + cid * hidden;
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int v = threadIdx.x + k * blockDim.x;
-    if (v < nv) {
-#pragma unroll
-      for (int e = 0; e < E; e += 4)
-        *reinterpret_cast<float4*>(pr + (base + v) * E + e) =
-            make_float4(acc[k][e], acc[k][e + 1], acc[k][e + 2], acc[k][e + 3]);
-    }
+   }
+    flush_partial<VPT, E>(acc, partial, part, hidden, base * E, threadIdx.x, blockDim.x, nv);
   }
 }
 
@@ -271,7 +268,7 @@ bool try_fwd_cluster_t(const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
 }
 
 template <typename T>
-bool try_bwd_cluster_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+bool try_bwd_cluster_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
   const int nvec = a.hidden / E;
   // up to 512 threads x 2 vectors per CTA
@@ -286,15 +283,15 @@ bool try_bwd_cluster_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* 
   // a persistent grid: as many clusters as can be resident at once
   int active = 0;
   if ((*err = max_active_clusters(kern, threads, csize, dev, &active)) != cudaSuccess) return true;
-  int64_t nclusters = active;
-  if (nclusters < 1) nclusters = 1;
-  if (nclusters > a.rows) nclusters = a.rows;
-  if (nclusters > a.max_partials) nclusters = a.max_partials;
-  *nparts = (int)nclusters;
-  *err = launch_clustered(kern, (unsigned)(nclusters * csize), threads, csize, s,
+  // the SM budget, in clusters
+  const int budget = sm_count(dev) / csize;
+  if (active > budget) active = budget > 0 ? budget : 1;
+  const BlockPlan bp = plan_blocks(a.rows, a.block_rows, unit_cap(a, active));
+  *nparts = bp.nblocks;
+  *err = launch_clustered(kern, (unsigned)(bp.units * csize), threads, csize, s,
                           static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
                           static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx),
-                          a.partial, a.rows, a.hidden, a.offset ? 1.f : 0.f, csize);
+                          a.partial, a.rows, a.hidden, a.offset ? 1.f : 0.f, csize, bp.brows);
   return true;
 }
 
@@ -310,7 +307,7 @@ bool try_launch_fwd_cluster(int dtype, const FwdArgs& a, cudaStream_t s, cudaErr
 }
 
 bool try_launch_bwd_cluster(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
-                            int* nparts) {
+                            int64_t* nparts) {
   if (!a.vec_ok) return false;
   switch (dtype) {
     case 0: return try_bwd_cluster_t<float>(a, s, err, nparts);

@@ -238,9 +238,114 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ---------------------------------------------------------------------------
+// fixed row blocks of the backward's weight gradient
+// ---------------------------------------------------------------------------
+// Every block of rows gets its own fp32 partial row of the weight gradient
+// -- the sum over the block's rows, in row order -- so the partials depend
+// only on where the blocks are, never on how many CTAs share the work.
+// Two layouts:
+//   brows > 0  blocks of `brows` consecutive rows (the last may be shorter);
+//              unit u of `units` persistent units (CTAs, or clusters of
+//              CTAs) owns the contiguous blocks [u*P/units, (u+1)*P/units)
+//              of the P blocks;
+//   brows == 0 one block per unit: unit u owns the rows [u*R/units,
+//              (u+1)*R/units), an even split.
+// Either way the unit owns the rows [r0, r0 + n) and its first block is
+// partial row b0.
+struct RowBlocks {
+  int64_t r0;    // first row
+  int n;         // rows owned (0 when the unit has no block)
+  int64_t b0;    // first block: partial row b0 holds the first block's sum
+  int brows;     // rows per block (the last block of the rows may be shorter)
+  __device__ __forceinline__ int64_t row(int i) const { return r0 + i; }
+  // rows of the unit's block that starts at its row i
+  __device__ __forceinline__ int block_end(int i) const {
+    return n - i < brows ? n : i + brows;
+  }
+};
+
+__device__ __forceinline__ RowBlocks row_blocks(int64_t rows, int brows, int64_t unit,
+                                                int64_t units) {
+  RowBlocks r;
+  if (brows == 0) {
+    r.r0 = unit * rows / units;
+    r.n = (int)((unit + 1) * rows / units - r.r0);
+    r.b0 = unit;
+    r.brows = r.n > 0 ? r.n : 1;
+    return r;
+  }
+  const int64_t nb = (rows + brows - 1) / brows;
+  const int64_t b0 = unit * nb / units, b1 = (unit + 1) * nb / units;
+  r.b0 = b0;
+  r.brows = brows;
+  r.r0 = b0 * brows;
+  const int64_t end = b1 * brows < rows ? b1 * brows : rows;
+  r.n = (int)(end > r.r0 ? end - r.r0 : 0);
+  return r;
+}
+
+// A thread's fp32 accumulators as its columns of partial row `part` (rows
+// of `hidden` floats, the unit's columns starting at col0), then zeroed.
+// The thread owns the 16-byte vectors first, first + stride, ... (VPT of
+// them, those below nvec), E floats each.
+template <int VPT, int E>
+__device__ __forceinline__ void flush_partial(float (&acc)[VPT][E], float* __restrict__ partial,
+                                              int64_t part, int64_t hidden, int64_t col0,
+                                              int first, int stride, int nvec) {
+  float* pr = partial + part * hidden + col0;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = first + k * stride;
+    if (v < nvec) {
+#pragma unroll
+      for (int i = 0; i < E; i += 4)
+        *reinterpret_cast<float4*>(pr + (int64_t)v * E + i) =
+            make_float4(acc[k][i], acc[k][i + 1], acc[k][i + 2], acc[k][i + 3]);
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[k][i] = 0.f;
+  }
+}
+
 // Correctly rounded 1/sqrt(v).
 __device__ __forceinline__ float rstd_of(float mean_sq, float eps) {
   return __frsqrt_rn(mean_sq + eps);
+}
+
+// Sums of squares past the fp32 range.  The statistics are fp32, and a row
+// of finite values can still overflow an fp32 sum of squares: |x| beyond
+// about 2^64 / sqrt(hidden), which bf16 and fp32 inputs can reach (fp16
+// cannot).  Such a row -- its sum is infinite -- is summed again with every
+// element scaled by s = 2^-73, and
+//   rstd = s / sqrt(sum (x s)^2 / hidden + eps s^2),
+// a power-of-two scaling that changes nothing but the range: the overflow
+// needs max |x| >= 2^64 / sqrt(65536) = 2^56, so the largest scaled square
+// is at least 2^-34 (full precision), and with |x| < 2^128 at most 2^110, so
+// 65536 of them stay below 2^127.  A row holding an infinity still sums to
+// infinity and keeps rstd = 0; a NaN propagates (its sum is NaN, not
+// infinite), as IEEE arithmetic gives.  Ordinary rows never take this
+// branch.
+constexpr float kOverflowScale = 0x1p-73f;
+
+__device__ __forceinline__ float rstd_rescaled(float ss_scaled, int hidden, float eps) {
+  const float s = kOverflowScale;
+  return rstd_of(ss_scaled / (float)hidden, eps * s * s) * s;
+}
+
+// This thread's share of sum (x s)^2 over the n elements of a row: elements
+// first, first + stride, ..., read again from memory one at a time (the
+// rare branch above, written to hold as few registers as it can).
+template <typename T>
+__device__ __forceinline__ float scaled_sum_sq(const T* __restrict__ xr, int first, int stride,
+                                               int n) {
+  float s2 = 0.f;
+#pragma unroll 1
+  for (int j = first; j < n; j += stride) {
+    const float t = Traits<T>::to_f(xr[j]) * kOverflowScale;
+    s2 = fmaf(t, t, s2);
+  }
+  return s2;
 }
 
 }  // namespace rmsn

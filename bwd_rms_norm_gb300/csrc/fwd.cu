@@ -22,6 +22,14 @@
 namespace rmsn {
 namespace {
 
+// rstd of a warp's row whose fp32 sum of squares overflowed (kOverflowScale),
+// out of line: the rare branch costs the ordinary path no registers.
+template <typename T>
+__device__ __noinline__ float rstd_overflow_warp(const T* __restrict__ xr, int lane, int hidden,
+                                                 float eps) {
+  return rstd_rescaled(warp_sum(scaled_sum_sq(xr, lane, 32, hidden)), hidden, eps);
+}
+
 // Output of one vector of x (already unpacked) for the chosen store.
 template <typename T>
 __device__ __forceinline__ uint4 scale_vec(const float (&xf)[Traits<T>::kVec],
@@ -60,7 +68,7 @@ __device__ __forceinline__ void store_vec(void* y, int64_t elem,
 }
 
 template <typename T, int VPT, bool F8>
-__global__ void __launch_bounds__(256) fwd_warp_rows(
+__global__ void __launch_bounds__(256, 5) fwd_warp_rows(
     const T* __restrict__ x, const T* __restrict__ gamma, void* __restrict__ y,
     float* __restrict__ rstd, int64_t rows, int hidden, float eps, float off,
     int twice, const float* __restrict__ scale) {
@@ -89,7 +97,9 @@ __global__ void __launch_bounds__(256) fwd_warp_rows(
     for (int i = 0; i < E; ++i) ss = fmaf(f[i], f[i], ss);
   }
   ss = warp_sum(ss);
-  const float rs = rstd_of(ss / (float)hidden, eps);
+  float rs = rstd_of(ss / (float)hidden, eps);
+  if (isinf(ss))  // the fp32 sum of squares overflowed (see kOverflowScale)
+    rs = rstd_overflow_warp(xr, lane, hidden, eps);
   if (lane == 0) rstd[row] = rs;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
@@ -104,7 +114,7 @@ __global__ void __launch_bounds__(256) fwd_warp_rows(
 }
 
 template <typename T, int VPT, bool F8>
-__global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) fwd_cta_row(
+__global__ void __launch_bounds__(VPT >= 8 ? 512 : VPT >= 4 ? 1024 : 128, VPT <= 2 ? 16 : 1) fwd_cta_row(
     const T* __restrict__ x, const T* __restrict__ gamma, void* __restrict__ y,
     float* __restrict__ rstd, int hidden, float eps, float off, int twice,
     const float* __restrict__ scale) {
@@ -132,7 +142,10 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) fwd_cta_row(
     for (int i = 0; i < E; ++i) ss = fmaf(f[i], f[i], ss);
   }
   ss = block_sum(ss, red, 0);
-  const float rs = rstd_of(ss / (float)hidden, eps);
+  float rs = rstd_of(ss / (float)hidden, eps);
+  if (isinf(ss))  // the fp32 sum of squares overflowed (see kOverflowScale)
+    rs = rstd_rescaled(block_sum(scaled_sum_sq(xr, threadIdx.x, blockDim.x, hidden), red, 1),
+                       hidden, eps);
   if (threadIdx.x == 0) rstd[row] = rs;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
@@ -163,7 +176,10 @@ __global__ void __launch_bounds__(256) fwd_scalar(
     ss = fmaf(f, f, ss);
   }
   ss = block_sum(ss, red, 0);
-  const float rs = rstd_of(ss / (float)hidden, eps);
+  float rs = rstd_of(ss / (float)hidden, eps);
+  if (isinf(ss))  // the fp32 sum of squares overflowed (see kOverflowScale)
+    rs = rstd_rescaled(block_sum(scaled_sum_sq(xr, threadIdx.x, blockDim.x, hidden), red, 1),
+                       hidden, eps);
   if (threadIdx.x == 0) rstd[row] = rs;
   for (int j = threadIdx.x; j < hidden; j += blockDim.x) {
     const float xh = Traits<T>::to_f(xr[j]) * rs;

@@ -38,7 +38,43 @@ struct BwdArgs {
   bool vec_ok;
   float* partial;          // fp32 workspace, >= max_partials * hidden floats
   int64_t max_partials;    // partial rows the workspace holds
+  int64_t block_rows;      // rows per weight-gradient partial; 0: one block per
+                           // CTA (or cluster) of the launch
+  float* chunks;           // non-NULL: write the chunk sums [ceil(P / 32), hidden]
+                           // here instead of reducing them into dw
 };
+
+// Rows per block, number of blocks (partial rows) and persistent units of
+// a backward launch.  block_rows 0: one block per unit, the rows split
+// evenly over min(rows, max_units) units (the kernels' brows 0).
+struct BlockPlan {
+  int brows;
+  int64_t nblocks;
+  int units;
+};
+
+inline BlockPlan plan_blocks(int64_t rows, int64_t block_rows, int64_t max_units) {
+  if (max_units < 1) max_units = 1;
+  BlockPlan p;
+  if (block_rows <= 0) {
+    p.brows = 0;
+    p.units = (int)(rows < max_units ? rows : max_units);
+    p.nblocks = p.units;
+    return p;
+  }
+  p.brows = (int)block_rows;
+  p.nblocks = (rows + block_rows - 1) / block_rows;
+  p.units = (int)(p.nblocks < max_units ? p.nblocks : max_units);
+  return p;
+}
+
+// Units a backward launch may use when up to `resident` fit on the GPU at
+// once: with default blocks also limited by the partial rows the workspace
+// holds (one per unit).
+inline int64_t unit_cap(const BwdArgs& a, int64_t resident) {
+  if (a.block_rows == 0 && resident > a.max_partials) return a.max_partials;
+  return resident;
+}
 
 // dtype: 0 fp32, 1 bf16, 2 fp16.  Each returns the CUDA status of its
 // launches and adds the number of kernels it enqueued to *launches.
@@ -50,12 +86,12 @@ cudaError_t launch_bwd(int dtype, const BwdArgs& a, cudaStream_t s, int* launche
 // true with the launch status in *err (and the partial count in *nparts).
 bool try_launch_fwd_tma(int dtype, const FwdArgs& a, cudaStream_t s, cudaError_t* err);
 bool try_launch_bwd_tma(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
-                        int* nparts);
+                        int64_t* nparts);
 
 // Cluster kernels for wide rows (cluster.cu), same contract.
 bool try_launch_fwd_cluster(int dtype, const FwdArgs& a, cudaStream_t s, cudaError_t* err);
 bool try_launch_bwd_cluster(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
-                            int* nparts);
+                            int64_t* nparts);
 
 // The kernels the current C-ABI call on this thread has launched, in order
 // (the first four), for rms_norm_last_kernels().  capi.cu.
@@ -104,10 +140,20 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 }
 
 // out[j] = sum over the nparts rows of the fp32 matrix `partial`
-// [nparts, ncols] in a fixed order; column j goes to out0[j] for j < split,
-// to out1[j - split] otherwise (skipped when out1 is NULL).  bwd.cu.
-cudaError_t launch_column_sums(const float* partial, int nparts, int ncols, float* out0,
+// [nparts, ncols] in a fixed order -- chunks of 32 consecutive rows as a
+// pairwise tree, the chunk sums added in chunk order; column j goes to
+// out0[j] for j < split, to out1[j - split] otherwise (skipped when out1 is
+// NULL).  bwd.cu.
+cudaError_t launch_column_sums(const float* partial, int64_t nparts, int ncols, float* out0,
                                float* out1, int split, cudaStream_t s);
+// The first half of that order alone: chunk c's tree sum to chunks[c][j].
+cudaError_t launch_chunk_sums(const float* partial, int64_t nparts, int ncols, float* chunks,
+                              cudaStream_t s);
+// The second half alone: out[j] = chunks[0][j] + chunks[1][j] + ... in
+// chunk order.
+cudaError_t launch_chunk_totals(const float* chunks, int64_t nchunks, int ncols, float* out,
+                                cudaStream_t s);
+constexpr int kChunkParts = 32;  // partial rows per chunk of the fixed order
 
 // Inputs of one LayerNorm call, already validated (rows >= 1).
 struct LnFwdArgs {
@@ -188,7 +234,8 @@ cudaError_t launch_gn_fwd(int dtype, const GnArgs& a, cudaStream_t s);
 cudaError_t read_gn_wait_timeouts(unsigned int* out);
 cudaError_t launch_gn_bwd(int dtype, const GnArgs& a, cudaStream_t s, int* launches);
 
-// Device properties, cached per device.
+// Device properties, cached per device.  sm_count honours the SM budget
+// set with rms_norm_set_sm_budget (capi.cu).
 int sm_count(int device);
 int max_blocks_per_sm(const void* func, int block, size_t smem);
 

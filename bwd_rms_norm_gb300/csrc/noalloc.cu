@@ -91,6 +91,8 @@ extern "C" int rms_norm_bwd_noalloc(const void* dy, const void* x, const void* g
   // the partial count rms_norm_bwd would use with a workspace of exactly
   // rms_norm_bwd_workspace_size bytes
   a.max_partials = (int64_t)(need / ((size_t)hidden * sizeof(float)));
+  a.block_rows = 0;
+  a.chunks = nullptr;
   int launches = 0;
   e = launch_bwd(dtype, a, st, &launches);
   if (e != cudaSuccess) return cuda_fail(e);

@@ -244,7 +244,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
         for (int e = 0; e < E; ++e) part[e] = fmaf(f[e], f[e], part[e]);
       }
       const float ss = warp_sum(pairwise<E>(part));
-      const float rs = rstd_of(ss / (float)hidden, eps);
+      float rs = rstd_of(ss / (float)hidden, eps);
+      if (isinf(ss)) {  // the fp32 sum of squares overflowed (see kOverflowScale)
+        float s2 = 0.f;
+        for (int v = lane; v < nvec; v += 32) {
+          float f[E];
+          unpack<T>(st[v], f);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float t = f[e] * kOverflowScale;
+            s2 = fmaf(t, t, s2);
+          }
+        }
+        rs = rstd_rescaled(warp_sum(s2), hidden, eps);
+      }
       if (lane == 0) {
         rstd[rw.row(i)] = rs;
         pipe.stat[pos.stage] = rs;
@@ -307,13 +320,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
 // Backward.  Reducer: c = sum(dy * gain * x * rstd) / hidden of its row,
 // reading the fp32 gains from a shared-memory copy.  Appliers: dx =
 // rstd * (dy * gain - x_hat * c) for their vectors of every row, and the
-// fp32 dw accumulators of those columns, written once at the end as the
-// CTA's partial row.
+// fp32 dw accumulators of those columns, written as the block's partial
+// row at the end of every block of rows (RowBlocks).
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
-    int64_t rows, int hidden, float off, int stages, int reducers) {
+    int64_t rows, int hidden, float off, int stages, int reducers, int brows) {
   constexpr int E = Traits<T>::kVec;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Pipe pipe;
@@ -323,7 +336,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   float* gain = reinterpret_cast<float*>(smem);
   unsigned char* ring = smem + gain_bytes;
   const int appliers = blockDim.x - 32 * (1 + reducers);
-  const Rows rw = cta_rows(rows);
+  const RowBlocks blk = row_blocks(rows, brows, blockIdx.x, gridDim.x);
+  const Rows rw{blk.r0, blk.n};
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
@@ -402,7 +416,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   }
   RingPos pos{0, 0u};
   float rs_next = n > 0 ? __ldg(rstd + rw.row(0)) : 0.f;
-  for (int i = 0; i < n; ++i) {
+  int64_t part = blk.b0;
+  for (int i = 0; i < n; ++part) {
+   const int end = blk.block_end(i);
+   for (; i < end; ++i) {
     const float rs = rs_next;
     if (i + 1 < n) rs_next = __ldg(rstd + rw.row(i + 1));
     bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
@@ -430,17 +447,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
     __syncwarp();
     if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
     pos.advance(1, stages);
-  }
-  float* pr = partial + (int64_t)blockIdx.x * hidden;
-#pragma unroll
-  for (int j = 0; j < VPT; ++j) {
-    const int v = a + j * appliers;
-    if (v < nvec) {
-#pragma unroll
-      for (int e = 0; e < E; e += 4)
-        *reinterpret_cast<float4*>(pr + (int64_t)v * E + e) =
-            make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
-    }
+   }
+    flush_partial<VPT, E>(acc, partial, part, hidden, 0, a, appliers, nvec);
   }
 }
 
@@ -739,7 +747,7 @@ template <typename T>
 __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
-    int64_t rows, int hidden, float off, int stages, int reducers) {
+    int64_t rows, int hidden, float off, int stages, int reducers, int brows) {
   constexpr int E = Traits<T>::kVec;
   constexpr int VPT = 4;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -748,7 +756,8 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
   const int stride = (2 * row_bytes + 127) / 128 * 128;
   unsigned char* ring = smem;
   const int appliers = blockDim.x - 32 * (1 + reducers * kWideTeam);
-  const Rows rw = cta_rows(rows);
+  const RowBlocks blk = row_blocks(rows, brows, blockIdx.x, gridDim.x);
+  const Rows rw{blk.r0, blk.n};
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
@@ -829,7 +838,9 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
   }
   RingPos pos{0, 0u};
   float rs_next = n > 0 ? __ldg(rstd + rw.row(0)) : 0.f;
-  for (int i = 0; i < n; ++i) {
+  int64_t part = blk.b0;
+  for (int i = 0; i < n; ++part) {
+   for (const int end = blk.block_end(i); i < end; ++i) {
     const float rs = rs_next;
     if (i + 1 < n) rs_next = __ldg(rstd + rw.row(i + 1));
     bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
@@ -861,17 +872,8 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
     __syncwarp();
     if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
     pos.advance(1, stages);
-  }
-  float* pr = partial + (int64_t)blockIdx.x * hidden;
-#pragma unroll
-  for (int j = 0; j < VPT; ++j) {
-    const int v = a + j * appliers;
-    if (v < nvec) {
-#pragma unroll
-      for (int e = 0; e < E; e += 4)
-        *reinterpret_cast<float4*>(pr + (int64_t)v * E + e) =
-            make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
-    }
+   }
+    flush_partial<VPT, E>(acc, partial, part, hidden, 0, a, appliers, nvec);
   }
 }
 
@@ -988,18 +990,25 @@ bool try_fwd_tma_t(const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
 }
 
 template <typename T, int VPT>
-cudaError_t launch_bwd_tma_v(const BwdArgs& a, int appliers, int stages, int reducers, int grid,
-                             cudaStream_t s) {
+cudaError_t launch_bwd_tma_v(const BwdArgs& a, int appliers, int stages, int reducers,
+                             const BlockPlan& bp, cudaStream_t s) {
   auto kern = bwd_tma<T, VPT>;
   const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
   cudaError_t e = allow_smem((const void*)kern);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, dim3(grid), dim3(32 * (1 + reducers) + appliers),
+  return launch_kernel(kern, dim3(bp.units), dim3(32 * (1 + reducers) + appliers),
                        (size_t)gain_bytes + (size_t)stages * stride, s, 1,
                        static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
                        static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
-                       a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers);
+                       a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers, bp.brows);
+}
+
+// The block plan of a persistent backward with one CTA per SM.
+BlockPlan bwd_plan(const BwdArgs& a, cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  return plan_blocks(a.rows, a.block_rows, unit_cap(a, sm_count(dev)));
 }
 
 // Backward for wide rows over a cluster of csize (2 or 4) CTAs: CTA q of
@@ -1021,7 +1030,7 @@ template <typename T, int CS>
 __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
-    int64_t rows, int hidden, float off, int stages, int reducers) {
+    int64_t rows, int hidden, float off, int stages, int reducers, int brows) {
   constexpr int csize = CS;
   constexpr int E = Traits<T>::kVec;
   constexpr int VPT = 4;
@@ -1037,9 +1046,8 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
   unsigned char* ring = smem;
   const int appliers = blockDim.x - 32 * (1 + reducers * kWideTeam);
   const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
-  Rows rw;
-  rw.r0 = cid * rows / ncl;
-  rw.n = (int)((cid + 1) * rows / ncl - rw.r0);
+  const RowBlocks blk = row_blocks(rows, brows, cid, ncl);
+  const Rows rw{blk.r0, blk.n};
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
   if (threadIdx.x < 6) mbar_init(&xbar[threadIdx.x / 2][threadIdx.x % 2], csize);
@@ -1140,12 +1148,14 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
     RingPos pos{0, 0u};
     float rs_next = n > 0 ? __ldg(rstd + rw.row(0)) : 0.f;
     bool ok = true;
-    for (int i = 0; i < n && ok; ++i) {
+    int64_t part = blk.b0;
+    for (int i = 0; i < n && ok; ++part) {
+     for (const int end = blk.block_end(i); i < end && ok; ++i) {
       const float rs = rs_next;
       if (i + 1 < n) rs_next = __ldg(rstd + rw.row(i + 1));
       ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
-      ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      ok = __all_sync(0xffffffffu, ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort));
+      if (!ok) break;
       const float c = pipe.stat[pos.stage];
       const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
       T* dxr = dx + rw.row(i) * hidden + col0;
@@ -1171,19 +1181,8 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
       __syncwarp();
       if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
       pos.advance(1, stages);
-    }
-    if (ok) {
-      float* pr = partial + cid * hidden + col0;
-#pragma unroll
-      for (int j = 0; j < VPT; ++j) {
-        const int v = a + j * appliers;
-        if (v < nvec) {
-#pragma unroll
-          for (int e = 0; e < E; e += 4)
-            *reinterpret_cast<float4*>(pr + (int64_t)v * E + e) =
-                make_float4(acc[j][e], acc[j][e + 1], acc[j][e + 2], acc[j][e + 3]);
-        }
-      }
+     }
+      if (ok) flush_partial<VPT, E>(acc, partial, part, hidden, col0, a, appliers, nvec);
     }
   }
   __syncwarp();
@@ -1199,7 +1198,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
 // six), having twice the arithmetic per staged byte.  False when none fits.
 
 template <typename T>
-bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
   const int reducers = 3;
   const int min_stages = sizeof(T) == 4 ? 6 : 3;
@@ -1240,14 +1239,18 @@ bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* np
     cudaGetLastError();
     return false;
   }
-  int64_t ncl = active;
-  if (ncl > a.rows) ncl = a.rows;
-  if (ncl > a.max_partials) ncl = a.max_partials;
-  *nparts = (int)ncl;
-  *err = launch_kernel(kern, dim3((unsigned)(csize * ncl)), dim3(threads), (size_t)stages * stride,
-                       s, csize, static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
-                       static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
-                       a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers);
+  // the SM budget, in clusters
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return true;
+  const int budget = sm_count(dev) / csize;
+  if (active > budget) active = budget > 0 ? budget : 1;
+  const BlockPlan bp = plan_blocks(a.rows, a.block_rows, unit_cap(a, active));
+  *nparts = bp.nblocks;
+  *err = launch_kernel(kern, dim3((unsigned)(csize * bp.units)), dim3(threads),
+                       (size_t)stages * stride, s, csize, static_cast<const T*>(a.dy),
+                       static_cast<const T*>(a.x), static_cast<const T*>(a.gamma), a.rstd,
+                       static_cast<T*>(a.dx), a.partial, a.rows, a.hidden,
+                       a.offset ? 1.f : 0.f, stages, reducers, bp.brows);
   return true;
 }
 
@@ -1255,7 +1258,7 @@ bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* np
 // vectors per applier within kWideThreads threads; false when that does not
 // fit either.
 template <typename T>
-bool try_bwd_wide_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+bool try_bwd_wide_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
   const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   const int stages = kRingBudget / stride >= 3 ? 3 : 0, reducers = 3;
@@ -1263,21 +1266,21 @@ bool try_bwd_wide_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* npa
   int appliers = 0;
   if (pick_vpt(a.hidden / E, kWideThreads - 32 * (1 + reducers * kWideTeam), 4, &appliers) != 4)
     return false;
-  const int grid = grid_for(a.rows, a.max_partials, err);
+  const BlockPlan bp = bwd_plan(a, err);
   if (*err != cudaSuccess) return true;
-  *nparts = grid;
+  *nparts = bp.nblocks;
   auto kern = bwd_tma_wide<T>;
   if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
-  *err = launch_kernel(kern, dim3(grid), dim3(32 * (1 + reducers * kWideTeam) + appliers),
+  *err = launch_kernel(kern, dim3(bp.units), dim3(32 * (1 + reducers * kWideTeam) + appliers),
                        (size_t)stages * stride, s, 1, static_cast<const T*>(a.dy),
                        static_cast<const T*>(a.x), static_cast<const T*>(a.gamma), a.rstd,
                        static_cast<T*>(a.dx), a.partial, a.rows, a.hidden,
-                       a.offset ? 1.f : 0.f, stages, reducers);
+                       a.offset ? 1.f : 0.f, stages, reducers, bp.brows);
   return true;
 }
 
 template <typename T>
-bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* nparts) {
+bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
   const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
@@ -1289,13 +1292,13 @@ bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int* npar
                              : pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 2,
                                         &appliers);
   if (vpt == 0) return try_bwd_wide_t<T>(a, s, err, nparts) || try_bwd_split_t<T>(a, s, err, nparts);
-  const int grid = grid_for(a.rows, a.max_partials, err);
+  const BlockPlan bp = bwd_plan(a, err);
   if (*err != cudaSuccess) return true;
-  *nparts = grid;
+  *nparts = bp.nblocks;
   if (vpt == 1)
-    *err = launch_bwd_tma_v<T, 1>(a, appliers, stages, reducers, grid, s);
+    *err = launch_bwd_tma_v<T, 1>(a, appliers, stages, reducers, bp, s);
   else
-    *err = launch_bwd_tma_v<T, 2>(a, appliers, stages, reducers, grid, s);
+    *err = launch_bwd_tma_v<T, 2>(a, appliers, stages, reducers, bp, s);
   return true;
 }
 
@@ -1384,7 +1387,7 @@ bool try_launch_fwd_tma(int dtype, const FwdArgs& a, cudaStream_t s, cudaError_t
 }
 
 bool try_launch_bwd_tma(int dtype, const BwdArgs& a, cudaStream_t s, cudaError_t* err,
-                        int* nparts) {
+                        int64_t* nparts) {
   if (!a.vec_ok) return false;
   switch (dtype) {
     case 0: return try_bwd_tma_t<float>(a, s, err, nparts);

@@ -109,16 +109,87 @@ size_t rms_norm_bwd_workspace_size(int64_t rows, int64_t hidden, int dtype);
  * The cast mode of the forward does not enter: the gradient is that of the
  * unrounded forward.  `workspace` is caller-owned device scratch of at least
  * rms_norm_bwd_workspace_size(rows, hidden, dtype) bytes, 16-byte aligned;
- * its contents need no initialisation and are clobbered.  dw is reduced from
- * per-block partials in a fixed order, so repeated calls with the same sizes
- * on the same GPU model give bit-identical results.  rows == 0 zero-fills dw
- * and returns RMSN_OK (dy, x, rstd, dx, workspace may then be NULL).
- * Outputs must not overlap inputs.
+ * its contents need no initialisation and are clobbered.  dw is reduced in a
+ * fixed order from fp32 partials over blocks of rows, one block per CTA of
+ * the launch (the rows split evenly over the CTAs, whose count the GPU's SM
+ * count and the SM budget set): partial b goes to lane b mod 16, each lane
+ * adds its partials in increasing b, and the 16 lane sums are added in
+ * order.  Repeated calls with the same sizes and SM budget therefore give
+ * bit-identical results.  rms_norm_bwd_blocked takes the
+ * block size from the caller instead, for results that do not depend on the
+ * GPU or on how the rows are split.  rows == 0 zero-fills dw and returns
+ * RMSN_OK (dy, x, rstd, dx, workspace may then be NULL).  Outputs must not
+ * overlap inputs.
  */
 int rms_norm_bwd(const void* dy, const void* x, const void* gamma,
                  const float* rstd, void* dx, float* dw,
                  int64_t rows, int64_t hidden, int offset, int dtype,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The weight gradient over caller-chosen row blocks, for results that do not
+ * depend on the GPU, on the SM budget, or on how the rows are split between
+ * calls or ranks.  The pages fix the precision of dw (fp32, Liger-Kernel PR
+ * #92, the author's comment after the benchmark tables) but not its
+ * summation order; this fixes one that every split can reproduce:
+ *
+ *   the rows are cut into blocks of `block_rows` consecutive rows (the last
+ *   may be shorter); block b's partial is sum over its rows, in row order, of
+ *   dy * x_hat in fp32;
+ *   the block partials form chunks of RMSN_DW_CHUNK_BLOCKS (32) consecutive
+ *   blocks (the last may be shorter); with p_k the chunk's k-th partial (a
+ *   missing one counting as +0) and s_t = p_t + p_(t+16), the chunk's sum is
+ *   ((s_0 + s_1) + s_2) + ... + s_15;
+ *   dw = ((chunk 0's sum + chunk 1's sum) + chunk 2's sum) + ... in chunk
+ *   order.
+ *
+ * rms_norm_bwd_blocked computes dx (as rms_norm_bwd) and the chunk sums of
+ * its rows into chunk_sums [rms_norm_dw_chunk_count(rows, block_rows),
+ * hidden] fp32 (device, caller-owned, overwritten); rms_norm_dw_sum adds
+ * nchunks chunk sums [nchunks, hidden] in order into dw [hidden] (nchunks
+ * == 0 zero-fills dw).  One call over all rows followed by rms_norm_dw_sum
+ * gives the same bits as any split of the rows into runs of whole chunks --
+ * one call per run, the runs' chunk sums laid end to end in row order --
+ * followed by rms_norm_dw_sum: a data-parallel job gathers the ranks' chunk
+ * sums (e.g. an all-gather) instead of summing their dw.
+ * rms_norm_rank_rows gives rank `rank` of `world` its slab of `rows` rows:
+ * [*row_lo, *row_hi), whole chunks, the chunks split as evenly as possible
+ * (a slab may be empty when there are fewer chunks than ranks).
+ *
+ * `workspace` holds the block partials:
+ * rms_norm_bwd_blocked_workspace_size(rows, hidden, block_rows) bytes,
+ * 16-byte aligned, contents clobbered.  block_rows >= 1 (RMSN_ERR_ARG
+ * otherwise).  The kernels deal whole blocks to CTAs: a block of more rows
+ * than an even split of the rows over the SMs would give one SM leaves SMs
+ * idle, and small blocks cost partial traffic (4 * hidden bytes per block,
+ * written and read once).  rows == 0 enqueues nothing (0 chunks).
+ * rms_norm_dw_chunk_count returns -RMSN_ERR_SHAPE for invalid arguments, the
+ * workspace size 0.  Errors otherwise as rms_norm_bwd.
+ */
+#define RMSN_DW_CHUNK_BLOCKS 32
+size_t rms_norm_bwd_blocked_workspace_size(int64_t rows, int64_t hidden, int64_t block_rows);
+int64_t rms_norm_dw_chunk_count(int64_t rows, int64_t block_rows);
+int rms_norm_bwd_blocked(const void* dy, const void* x, const void* gamma,
+                         const float* rstd, void* dx, float* chunk_sums,
+                         int64_t rows, int64_t hidden, int64_t block_rows,
+                         int offset, int dtype, void* workspace,
+                         size_t workspace_bytes, void* stream);
+int rms_norm_dw_sum(const float* chunk_sums, int64_t nchunks, int64_t hidden,
+                    float* dw, void* stream);
+int rms_norm_rank_rows(int64_t rows, int64_t block_rows, int world, int rank,
+                       int64_t* row_lo, int64_t* row_hi);
+
+/*
+ * SM budget: the persistent kernels of every entry point launch at most as
+ * many CTAs as `sms` SMs hold resident at once (one per SM for the staged
+ * kernels), which leaves the other SMs to work running beside them on other
+ * streams (a collective, a GEMM).  0 (the default) uses every SM.  A
+ * process-wide setting read at each launch; change it between calls, not
+ * during them.  The pages describe no such knob.  Returns RMSN_ERR_ARG for
+ * sms < 0; rms_norm_sm_budget returns the current setting.
+ */
+int rms_norm_set_sm_budget(int sms);
+int rms_norm_sm_budget(void);
 
 /*
  * RMSNorm forward with an FP8 output and a per-tensor scale ("Den dolda

@@ -49,7 +49,7 @@ def test_header_constants_match_binding():
     consts = dict(re.findall(r"(RMSN_\w+)\s*=\s*(\d+)", text))
     consts.update(dict(re.findall(r"#define\s+(RMSN_\w+)\s+(\d+)", text)))
     for name in ("RMSN_F32", "RMSN_BF16", "RMSN_F16", "RMSN_ROUND_ONCE", "RMSN_ROUND_TWICE",
-                 "RMSN_OK", "RMSN_MAX_HIDDEN", "RMSN_MAX_PARTIALS"):
+                 "RMSN_OK", "RMSN_MAX_HIDDEN", "RMSN_MAX_PARTIALS", "RMSN_DW_CHUNK_BLOCKS"):
         assert int(consts[name]) == getattr(L, name), name
 
 
@@ -244,3 +244,65 @@ def test_rms_norm_module_host_side():
         L.RMSNorm(16, cast_mode="round_thrice")
     with pytest.raises(RuntimeError, match="CUDA"):
         m(torch.zeros(3, 16, requires_grad=True))
+
+
+def test_blocked_backward_validation(lib):
+    """The fixed-block backward and the chunk total refuse bad arguments
+    before any CUDA call."""
+    ws = lib.rms_norm_bwd_blocked_workspace_size(100, 64, 8)
+    assert ws == 13 * 64 * 4                       # ceil(100 / 8) partial rows
+    assert lib.rms_norm_bwd_blocked_workspace_size(100, 64, 0) == 0
+    assert lib.rms_norm_dw_chunk_count(100, 8) == 1
+    assert lib.rms_norm_dw_chunk_count(32 * 8 + 1, 8) == 2
+    assert lib.rms_norm_dw_chunk_count(0, 8) == 0
+    assert lib.rms_norm_dw_chunk_count(10, 0) == -2
+
+    def call(rows=100, hidden=64, brows=8, chunks=FAKE, ws_bytes=ws, dtype=1, offset=0):
+        return lib.rms_norm_bwd_blocked(FAKE, FAKE, FAKE, FAKE, FAKE, chunks, rows, hidden, brows,
+                                        offset, dtype, FAKE, ws_bytes, None)
+
+    assert call(brows=0) == 8                      # RMSN_ERR_ARG
+    assert call(rows=-1) == 2                      # RMSN_ERR_SHAPE
+    assert call(hidden=0) == 2
+    assert call(dtype=7) == 4
+    assert call(offset=2) == 8
+    assert call(chunks=None) == 1                  # RMSN_ERR_NULL
+    assert call(ws_bytes=ws - 4) == 6              # RMSN_ERR_WORKSPACE
+    assert call(rows=0) == 0                       # nothing to do
+    assert lib.rms_norm_dw_sum(FAKE, -1, 64, FAKE, None) == 2
+    assert lib.rms_norm_dw_sum(FAKE, 3, 0, FAKE, None) == 2
+    assert lib.rms_norm_dw_sum(FAKE, 3, 64, None, None) == 1
+    assert lib.rms_norm_dw_sum(None, 3, 64, FAKE, None) == 1
+
+
+@pytest.mark.parametrize("rows,brows", [(0, 4), (1, 4), (1000, 4), (16384, 16), (4097, 1),
+                                        (12345, 7)])
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+def test_rank_rows_are_whole_chunks(lib, rows, brows, world):
+    """rms_norm_rank_rows tiles the rows with contiguous slabs whose
+    boundaries are whole chunks (32 blocks), as evenly as the chunks allow."""
+    lo, hi = ctypes.c_int64(), ctypes.c_int64()
+    spans = []
+    for r in range(world):
+        assert lib.rms_norm_rank_rows(rows, brows, world, r, ctypes.byref(lo),
+                                      ctypes.byref(hi)) == 0
+        spans.append((lo.value, hi.value))
+    assert spans[0][0] == 0 and spans[-1][1] == rows
+    chunk = 32 * brows
+    for (a, b), (c, _) in zip(spans, spans[1:]):
+        assert b == c
+        assert b % chunk == 0 or b == rows
+    counts = [-(-(b - a) // chunk) for a, b in spans]
+    assert max(counts) - min(counts) <= 1
+    assert lib.rms_norm_rank_rows(rows, brows, world, world, ctypes.byref(lo),
+                                  ctypes.byref(hi)) == 8
+    assert lib.rms_norm_rank_rows(rows, 0, world, 0, ctypes.byref(lo), ctypes.byref(hi)) == 8
+
+
+def test_sm_budget_setting(lib):
+    assert lib.rms_norm_sm_budget() == 0
+    assert lib.rms_norm_set_sm_budget(-1) == 8
+    assert lib.rms_norm_set_sm_budget(100) == 0
+    assert lib.rms_norm_sm_budget() == 100
+    assert lib.rms_norm_set_sm_budget(0) == 0
+    assert lib.rms_norm_sm_budget() == 0
