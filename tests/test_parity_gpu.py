@@ -94,6 +94,27 @@ def test_fp16_overflow_stress(L):
         run_and_check(L, w)
 
 
+@pytest.mark.parametrize("rows,hidden,dtype", [
+    (64, 1024, "bf16"), (40, 2048, "f32"), (24, 4096, "bf16"), (16, 8192, "f32"),
+    (12, 16384, "bf16"), (6, 65536, "f32"), (10, 1001, "bf16"), (8, 3, "f32")])
+def test_sum_of_squares_past_fp32(L, rows, hidden, dtype):
+    """Rows of bf16/fp32 values so large that an fp32 sum of squares
+    overflows (every square past 2**128 for the 2**70 rows; only the sum for
+    the 2**60 rows), beside ordinary rows and rows near 2**100: the kernels
+    sum those rows again scaled by a power of two, so rstd, y and the
+    backward match the float64 oracle, whose squares never overflow."""
+    w = W.Workload("overflow", rows, hidden, dtype, 1e-5, 0, "round_once",
+                   ("normal", 0.0, 1.0), ("uniform", 0.9, 1.1), ("normal", 0.0, 1.0),
+                   seed=rows + hidden)
+    inp = W.make_inputs(w)
+    scale = torch.tensor([2.0 ** (70, 60, 0, 100)[r % 4] for r in range(rows)])
+    inp["x"] = (inp["x"].double() * scale[:, None]).to(inp["x"].dtype)
+    assert torch.isfinite(inp["x"]).all()
+    x32 = inp["x"].float()
+    assert torch.isinf((x32 * x32).sum(dim=1)[0])      # the fp32 sum does overflow
+    run_and_check(L, w, inputs=inp)
+
+
 SHAPES = [
     # rows, hidden, dtype -- covers warp-per-row, CTA-per-row, 16-vector
     # rows, the scalar path (hidden not a multiple of the vector), widths
