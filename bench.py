@@ -59,6 +59,9 @@ def metric_for(w) -> str:
     return {"ln": METRIC_LN, "softmax": METRIC_SM, "gn": METRIC_GN}.get(w.kind, METRIC)
 DEFAULT_WORKLOAD = "large_bf16_16384x8192_once"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+# Rows per weight-gradient block of the data-parallel exchange (a chunk is
+# 32 blocks): the largest of these whose chunk divides a rank's rows.
+DP_BLOCK_ROWS = (16, 8, 4, 2, 1)
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -409,6 +412,33 @@ def run_ours(args, rank, world, local):
     ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
     half = nsets // 2
 
+    # Data parallel (more than one rank, or --dp-exchange): rank k's batch is
+    # slab k of a global batch of world x rows rows, cut by the library's
+    # rms_norm_rank_rows into whole chunks of 32 blocks; the backward leaves
+    # its slab's weight-gradient chunk sums, the ranks all-gather them and
+    # every rank adds them in chunk order -- the weight gradient of the
+    # global batch, the same bits for any number of ranks.
+    dp = (world > 1 or args.dp_exchange) and not (ln or sm or gn)
+    dp_info = None
+    if dp:
+        brows = next((b for b in DP_BLOCK_ROWS if w.rows % (32 * b) == 0), None)
+        if brows is None:
+            raise SystemExit(f"data-parallel exchange needs rows divisible by 32 "
+                             f"(a chunk of 32 one-row blocks), not {w.rows}")
+        lo, hi = L.rms_norm_rank_rows(w.rows * world, brows, world, rank)
+        assert (lo, hi) == (rank * w.rows, (rank + 1) * w.rows), (lo, hi)
+        nch = L.rms_norm_dw_chunk_count(w.rows, brows)
+        chunks = torch.empty(nch, w.hidden, dtype=torch.float32, device=dev)
+        gathered = (torch.empty(world * nch, w.hidden, dtype=torch.float32, device=dev)
+                    if world > 1 else chunks)
+        ws = torch.empty(max(16, L.rms_norm_bwd_blocked_workspace_size(w.rows, w.hidden, brows)),
+                         dtype=torch.uint8, device=dev)
+        import torch.distributed as dist
+        dp_info = {"block_rows": brows, "chunks_per_rank": nch, "global_rows": w.rows * world,
+                   "rank_rows": [lo, hi],
+                   "exchange": (f"all_gather of {nch} x {w.hidden} fp32 chunk sums per rank"
+                                if world > 1 else "none (one rank)")}
+
     def fwd(k):
         S = sets[k]
         if sm:
@@ -433,6 +463,12 @@ def run_ours(args, rank, world, local):
         elif ln:
             L.layer_norm_bwd(S["dy"], S["x"], g, S["mean"], S["rstd"], dx=S["dx"], dgamma=dw,
                              dbeta=db, workspace=ws)
+        elif dp:
+            L.rms_norm_bwd_blocked(S["dy"], S["x"], g, S["rstd"], dp_info["block_rows"],
+                                   w.offset, dx=S["dx"], chunk_sums=chunks, workspace=ws)
+            if world > 1:
+                dist.all_gather_into_tensor(gathered, chunks)
+            L.rms_norm_dw_sum(gathered, dw=dw)
         else:
             L.rms_norm_bwd(S["dy"], S["x"], g, S["rstd"], w.offset, dx=S["dx"], dw=dw,
                            workspace=ws)
@@ -442,6 +478,26 @@ def run_ours(args, rank, world, local):
         fwd(i % nsets)
         bwd((i + half) % nsets)
 
+    if args.profile:
+        # eager steps only, for a profiler: warm-up steps, then the profiled
+        # ones, no graphs, no timing, nothing else launched
+        for i in range(args.warmup + args.steps):
+            step(i)
+            if i == args.warmup - 1:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        kernels = {}
+        fwd(0)
+        kernels["fwd"] = L.last_kernels()
+        bwd(0)
+        kernels["bwd"] = L.last_kernels()
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"profile": args.workload, "rows": w.rows, "hidden": w.hidden,
+                              "warmup_steps": args.warmup, "steps": args.steps,
+                              "sets": nsets, "kernels": kernels}), flush=True)
+        return
+
     # eager warm-up: every kernel configuration is set up before capture
     for i in range(max(args.warmup, nsets)):
         step(i)
@@ -450,10 +506,25 @@ def run_ours(args, rank, world, local):
     fwd(0)
     launches_per_step = L.last_launch_count()
     bwd(0)
-    launches_per_step += L.last_launch_count()
+    # data parallel: the last call is rms_norm_dw_sum; the blocked backward
+    # before it launched two kernels
+    launches_per_step += L.last_launch_count() + (2 if dp else 0)
     torch.cuda.synchronize()
 
+    class Eager:
+        """Stands in for a CUDA graph where the step holds a collective:
+        replay() launches the same calls eagerly."""
+
+        def __init__(self, fn, n):
+            self.fn, self.n = fn, n
+
+        def replay(self):
+            for i in range(self.n):
+                self.fn(i)
+
     def capture(fn, n):
+        if dp and world > 1:
+            return Eager(fn, n)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(n):
@@ -617,12 +688,19 @@ def run_ours(args, rank, world, local):
             **({"offset": w.offset, "cast_mode": w.cast_mode} if not (ln or sm or gn) else {}),
             **({"y": "fp8 e4m3 (saturating)", "scale": w.scale} if f8 else {}),
             "global_batch_rows": w.rows * world,
-            "parallelism": f"replica x{world} (one batch per rank)",
+            "parallelism": (f"data parallel x{world}: one slab of {w.rows} rows per rank of a "
+                            f"global batch of {w.rows * world} rows; weight gradient over the "
+                            f"global batch from all-gathered chunk sums" if dp else
+                            f"replica x{world} (one batch per rank)"),
+            **({"dp": dp_info} if dp else {}),
             "l2": (f"inputs larger than L2: {nsets} copies of the batch "
                    f"({nsets * set_bytes / 2**20:.0f} MiB) cycled; each step's backward "
                    f"reads the copy whose forward ran {half} steps earlier"),
             "timing": ("CUDA events around one CUDA-graph replay of exactly `steps` "
-                       "forward+backward steps (C-ABI calls captured in order)"),
+                       "forward+backward steps (C-ABI calls captured in order)"
+                       if not (dp and world > 1) else
+                       "CUDA events around exactly `steps` forward+backward steps launched "
+                       "eagerly (the step holds an NCCL all_gather), max over ranks"),
             "algorithmic_bytes_per_step": w.step_bytes(),
         },
         "fwd_us": round(fwd_us, 3),
@@ -946,6 +1024,10 @@ def main(argv=None):
                     help="override the workload's row count (profiling a larger case)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dp-exchange", action="store_true",
+                    help="on one rank, run the data-parallel weight-gradient path of N > 1")
+    ap.add_argument("--profile", action="store_true",
+                    help="run warm-up and steps eagerly and nothing else (for ncu)")
     ap.add_argument("--no-variant", action="store_true",
                     help="skip timing the other cast mode of a workload that has both")
     args = ap.parse_args(argv)
