@@ -163,6 +163,43 @@ __device__ __forceinline__ void produce(Pipe& p, unsigned char* ring, int stride
   produce_pitched<NSRC>(p, ring, stride, stages, src, rw, row_bytes, row_bytes, abort);
 }
 
+// Producer of stages that hold K consecutive rows each (narrow rows): stage
+// j takes the CTA's rows [jK, min(jK + K, n)).  A tensor's rows are
+// contiguous in global memory, so one bulk copy a tensor fills the stage;
+// tensor t's rows go to bytes [t * K * row_bytes, (t + 1) * K * row_bytes)
+// of the stage.  Copies and drain as in produce_pitched.
+template <int NSRC, int K>
+__device__ void produce_rows(Pipe& p, unsigned char* ring, int stride, int stages,
+                             const void* const (&src)[NSRC], const Rows& rw, uint32_t row_bytes,
+                             volatile int* abort) {
+  RingPos pos{0, 0u};
+  const int nst = (rw.n + K - 1) / K;
+  int j = 0;
+  for (; j < nst; ++j) {
+    if (j >= stages && !wait_phase(&p.empty[pos.stage], pos.phase ^ 1u, abort)) break;
+    const int i = j * K;
+    const uint32_t bytes = (uint32_t)(rw.n - i < K ? rw.n - i : K) * row_bytes;
+    unsigned char* dst = ring + (size_t)pos.stage * stride;
+    mbar_arrive_expect_tx(&p.full[pos.stage], NSRC * bytes);
+    const size_t off = (size_t)rw.row(i) * row_bytes;
+#pragma unroll
+    for (int t = 0; t < NSRC; ++t)
+      bulk_load(dst + (size_t)t * K * row_bytes, static_cast<const unsigned char*>(src[t]) + off,
+                bytes, &p.full[pos.stage]);
+    pos.advance(1, stages);
+  }
+  const int outstanding = j < stages ? j : stages;
+  for (int q = 0; q < outstanding; ++q) {
+    if (pos.stage == 0) {
+      pos.stage = stages - 1;
+      pos.phase ^= 1u;
+    } else {
+      --pos.stage;
+    }
+    drain_phase(&p.full[pos.stage], pos.phase);
+  }
+}
+
 // Sum of per-element partial sums, pairwise.
 template <int E>
 __device__ __forceinline__ float pairwise(float (&p)[E]) {
@@ -452,6 +489,159 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   }
 }
 
+
+// Backward for narrow rows, in stages of K consecutive rows (produce_rows).
+// One row a stage leaves such rows paced by handshakes rather than by
+// bandwidth: every row cost the producer an mbarrier arm and two bulk
+// copies, and every applier warp two waits and an arrive, against about a
+// hundred instructions of arithmetic.  The roles are those of bwd_tma, with
+// the producer's and the appliers' handshakes shared by a stage's K rows.
+// The reducers still take rows, not stages (reducer d: rows d, d + R, ...),
+// so that a stage's rows are reduced side by side; each writes its row's c
+// and rstd into the stage's slot for that row, and red[s] completes when
+// all K have (a last stage with fewer rows gets an arrival for each missing
+// row too, after its copy landed).  R divides the stage count, so reducer d
+// meets a stage again only at its own row K * stages later.  The appliers
+// (one 16-byte vector of every row a thread) walk the stage's rows in order,
+// so every dw accumulator still adds its rows in row order and the results
+// are bit for bit those of bwd_tma.  Blocks of rows (RowBlocks) are whole
+// stages: K divides brows.
+template <typename T, int K>
+__global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma_rows(
+    const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
+    const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
+    int64_t rows, int hidden, float off, int stages, int reducers, int brows) {
+  constexpr int E = Traits<T>::kVec;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Pipe pipe;
+  __shared__ float cst[kMaxStages * K], rst[kMaxStages * K];
+  const int row_bytes = hidden * (int)sizeof(T);
+  const int stride = (2 * K * row_bytes + 127) / 128 * 128;
+  const int gain_bytes = (hidden * 4 + 127) / 128 * 128;
+  float* gain = reinterpret_cast<float*>(smem);
+  unsigned char* ring = smem + gain_bytes;
+  const int appliers = blockDim.x - 32 * (1 + reducers);
+  const RowBlocks blk = row_blocks(rows, brows, blockIdx.x, gridDim.x);
+  const Rows rw{blk.r0, blk.n};
+  const int n = rw.n;
+  const int nst = (n + K - 1) / K;
+  if (threadIdx.x == 0) pipe.abort = 0;
+  if (threadIdx.x < stages) {
+    mbar_init(&pipe.full[threadIdx.x], 1);
+    mbar_init(&pipe.red[threadIdx.x], K);
+    mbar_init(&pipe.empty[threadIdx.x], K + appliers / 32);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  volatile int* abort = &pipe.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = hidden / E;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const void* const src[2] = {x, dy};
+      produce_rows<2, K>(pipe, ring, stride, stages, src, rw, (uint32_t)row_bytes, abort);
+    }
+    return;
+  }
+
+  if (warp <= reducers) {
+    stage_gains<T>(gain, gamma, nvec, off, threadIdx.x - 32, 32 * reducers);
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * reducers) : "memory");
+    const float4* g4 = reinterpret_cast<const float4*>(gain);
+    const int d = warp - 1;
+    // slot i: row i of the CTA, or a missing row of the last stage (i >= n)
+    for (int i = d; i < nst * K; i += reducers) {
+      const int j = i / K, r = i - j * K;
+      const int stage = j % stages;
+      const uint32_t phase = (uint32_t)(j / stages) & 1u;
+      const float rs = i < n ? __ldg(rstd + rw.row(i)) : 0.f;
+      if (!__all_sync(0xffffffffu, wait_phase(&pipe.full[stage], phase, abort))) return;
+      if (i < n) {
+        const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)stage * stride);
+        float part[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[e] = 0.f;
+#pragma unroll 2
+        for (int v = lane; v < nvec; v += 32) {
+          float xf[E], df[E], gf[E];
+          unpack<T>(st[r * nvec + v], xf);
+          unpack<T>(st[(K + r) * nvec + v], df);
+#pragma unroll
+          for (int e = 0; e < E; e += 4) {
+            const float4 q = g4[(e / 4) * nvec + v];
+            gf[e] = q.x;
+            gf[e + 1] = q.y;
+            gf[e + 2] = q.z;
+            gf[e + 3] = q.w;
+          }
+#pragma unroll
+          for (int e = 0; e < E; ++e) part[e] = fmaf(df[e] * gf[e], xf[e], part[e]);
+        }
+        // sum(g * x) * rstd: the row's rstd is applied once, to the sum
+        const float dot = warp_sum(pairwise<E>(part)) * rs;
+        if (lane == 0) {
+          cst[stage * K + r] = dot / (float)hidden;
+          rst[stage * K + r] = rs;
+        }
+      }
+      if (lane == 0) {
+        mbar_arrive(&pipe.red[stage]);
+        mbar_arrive(&pipe.empty[stage]);
+      }
+    }
+    return;
+  }
+
+  const int a = threadIdx.x - 32 * (1 + reducers);
+  float ge[E], acc[1][E];
+  {
+    const uint4 q = a < nvec ? ld_shared_ro(gamma + (int64_t)a * E) : make_uint4(0, 0, 0, 0);
+    unpack<T>(q, ge);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      ge[e] += off;
+      acc[0][e] = 0.f;
+    }
+  }
+  RingPos pos{0, 0u};
+  int64_t part = blk.b0;
+  int bend = blk.block_end(0);
+  for (int j = 0, i = 0; j < nst; ++j) {
+    const int k = n - i < K ? n - i : K;
+    bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
+    ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+#pragma unroll
+    for (int r = 0; r < K; ++r) {
+      if (r < k && a < nvec) {
+        const float c = cst[pos.stage * K + r], rs = rst[pos.stage * K + r];
+        float xf[E], df[E], o[E];
+        unpack<T>(st[r * nvec + a], xf);
+        unpack<T>(st[(K + r) * nvec + a], df);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float xh = xf[e] * rs;
+          acc[0][e] = fmaf(df[e], xh, acc[0][e]);
+          o[e] = fmaf(-xh, c, df[e] * ge[e]) * rs;
+        }
+        st_vec(dx + rw.row(i + r) * hidden + (int64_t)a * E, pack<T>(o));
+      }
+    }
+    i += k;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
+    pos.advance(1, stages);
+    if (i == bend) {
+      flush_partial<1, E>(acc, partial, part, hidden, 0, a, appliers, nvec);
+      ++part;
+      bend = blk.block_end(i);
+    }
+  }
+}
 
 // LayerNorm forward.  Reducer: mean, then sum((x - mean)^2) over the row in
 // the stage (two passes over shared memory), rstd; both to global and to
@@ -1279,9 +1469,50 @@ bool try_bwd_wide_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t*
   return true;
 }
 
+// Rows per stage of the narrow-row backward: four rows up to 2 KB, two up to
+// 4 KB, else one (bwd_tma); with caller-sized blocks, a divisor of the block.
+int rows_per_stage(int64_t row_bytes, int64_t block_rows) {
+  int k = row_bytes <= 2048 ? 4 : row_bytes <= 4096 ? 2 : 1;
+  if (block_rows > 0)
+    while (k > 1 && block_rows % k != 0) k /= 2;
+  return k;
+}
+
+template <typename T, int K>
+bool try_bwd_rows_k(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
+  constexpr int E = Traits<T>::kVec;
+  const int stride = (2 * K * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
+  int stages = 0, reducers = 0;
+  split_stages((kRingBudget - gain_bytes) / stride, &stages, &reducers);
+  const int appliers = ((int)(a.hidden / E) + 31) / 32 * 32;
+  if (stages < 3 || appliers > kMaxThreads - 32 * (1 + reducers)) return false;
+  const BlockPlan bp = bwd_plan(a, err);
+  if (*err != cudaSuccess) return true;
+  *nparts = bp.nblocks;
+  auto kern = bwd_tma_rows<T, K>;
+  if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
+  *err = launch_kernel(kern, dim3(bp.units), dim3(32 * (1 + reducers) + appliers),
+                       (size_t)gain_bytes + (size_t)stages * stride, s, 1,
+                       static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
+                       static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.partial,
+                       a.rows, a.hidden, a.offset ? 1.f : 0.f, stages, reducers, bp.brows);
+  return true;
+}
+
 template <typename T>
 bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
+  switch (rows_per_stage(a.hidden * (int64_t)sizeof(T), a.block_rows)) {
+    case 4:
+      if (try_bwd_rows_k<T, 4>(a, s, err, nparts)) return true;
+      break;
+    case 2:
+      if (try_bwd_rows_k<T, 2>(a, s, err, nparts)) return true;
+      break;
+    default:
+      break;
+  }
   const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
   int stages = 0, reducers = 0;

@@ -37,11 +37,14 @@ def L():
     lib.rms_norm_set_sm_budget(0)
 
 
-# rows, hidden, dtype, the kernel the backward runs
+# rows, hidden, dtype, the kernel the backward runs (for narrow rows: with
+# blocks of 3 rows, and with blocks of 16, whose stages hold several rows)
 CASES = [
     (600, 4096, "bf16", "bwd_tma"),
     (300, 8192, "bf16", "bwd_tma"),
-    (500, 256, "f32", "bwd_tma"),
+    (500, 256, "f32", ("bwd_tma", "bwd_tma_rows")),
+    (600, 1024, "bf16", ("bwd_tma", "bwd_tma_rows")),
+    (300, 2048, "f16", ("bwd_tma", "bwd_tma_rows")),
     (200, 16384, "f16", "bwd_tma_wide"),
     (100, 32768, "f16", "bwd_tma_split"),
     (90, 16384, "f32", "bwd_tma_split"),
@@ -83,6 +86,8 @@ def test_blocked_matches_oracle(L, rows, hidden, dtype, kernel, brows):
     offset = 1 if brows == 3 else 0
     w, (xd, gd, dyd, rstd_ref), dev = _setup(rows, hidden, dtype, offset)
     dx, chunks = _blocked(L, dev, brows, offset)
+    if isinstance(kernel, tuple):
+        kernel = kernel[0] if brows == 3 else kernel[1]
     ok, names = _ran(L, kernel)
     assert ok, names
     assert chunks.shape == (L.rms_norm_dw_chunk_count(rows, brows), hidden)
@@ -160,3 +165,22 @@ def test_empty_and_zero_chunk_calls(L):
 
 def test_no_bounded_wait_ran_out(L):
     assert L.wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("rows,hidden,dtype", [(600, 1024, "bf16"), (300, 2048, "f16"),
+                                               (500, 256, "f32"), (97, 512, "f16")])
+def test_multi_row_stages_give_the_one_row_kernels_dx(L, rows, hidden, dtype):
+    """Narrow rows are staged several to a ring slot (bwd_tma_rows) unless the
+    caller's blocks are not a multiple of the stage: blocks of 3 rows run the
+    one-row-a-stage kernel (bwd_tma).  dx does not depend on the blocks, so
+    the two kernels' dx must agree bit for bit, and with the default call."""
+    _, _, dev = _setup(rows, hidden, dtype)
+    dx3, _ = _blocked(L, dev, 3, 0)
+    assert _ran(L, "bwd_tma")[0]
+    dx16, _ = _blocked(L, dev, 16, 0)
+    assert _ran(L, "bwd_tma_rows")[0]
+    dx, _ = L.rms_norm_bwd(dev["dy"], dev["x"], dev["gamma"], dev["rstd"])
+    assert _ran(L, "bwd_tma_rows")[0]
+    torch.cuda.synchronize()
+    assert torch.equal(dx3, dx16)
+    assert torch.equal(dx3, dx)

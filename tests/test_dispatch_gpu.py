@@ -32,16 +32,18 @@ def _expect(names, *parts):
         assert p in n, (p, names)
 
 
-RMS = [  # workload, forward kernel, backward row kernel
-    ("llama_bf16_4096x4096", "fwd_tma", "bwd_tma"),
-    ("gemma_bf16_8192x3072", "fwd_tma", "bwd_tma"),
-    ("fp16_4096x1024", "fwd_warp_rows", "bwd_tma"),
-    ("fp16_4096x2048", "fwd_cta_row", "bwd_tma"),
-    ("fp16_4096x8192", "fwd_tma", "bwd_tma"),
+# workload, forward kernel, backward row kernel (a part of the mangled name:
+# "7bwd_tmaI" is bwd_tma itself, not bwd_tma_rows or bwd_tma_wide)
+RMS = [
+    ("llama_bf16_4096x4096", "fwd_tma", "7bwd_tmaI"),
+    ("gemma_bf16_8192x3072", "fwd_tma", "7bwd_tmaI"),
+    ("fp16_4096x1024", "fwd_warp_rows", "bwd_tma_rowsI6__halfLi4E"),
+    ("fp16_4096x2048", "fwd_cta_row", "bwd_tma_rowsI6__halfLi2E"),
+    ("fp16_4096x8192", "fwd_tma", "7bwd_tmaI"),
     ("fp16_4096x16384", "fwd_tma", "bwd_tma_wide"),
     ("fp16_4096x32768", "fwd_cta_row", "bwd_tma_split"),
-    ("large_bf16_16384x8192_once", "fwd_tma", "bwd_tma"),
-    ("fp32_256x1024", "fwd_cta_row", "bwd_tma"),
+    ("large_bf16_16384x8192_once", "fwd_tma", "7bwd_tmaI"),
+    ("fp32_256x1024", "fwd_cta_row", "bwd_tma_rowsIfLi2E"),
 ]
 
 
