@@ -133,6 +133,55 @@ __device__ __forceinline__ void unpack<__half>(const uint4& v, float (&f)[8]) {
   }
 }
 
+// Half vectors (8 bytes, kVec / 2 elements), for threads that own a
+// narrower slice of a row.
+template <typename T>
+__device__ __forceinline__ void unpack_h(const uint2& v, float (&f)[Traits<T>::kVec / 2]);
+
+template <>
+__device__ __forceinline__ void unpack_h<float>(const uint2& v, float (&f)[2]) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+}
+
+template <>
+__device__ __forceinline__ void unpack_h<__nv_bfloat16>(const uint2& v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+
+template <>
+__device__ __forceinline__ void unpack_h<__half>(const uint2& v, float (&f)[4]) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  f[0] = a.x;
+  f[1] = a.y;
+  f[2] = b.x;
+  f[3] = b.y;
+}
+
+template <typename T>
+__device__ __forceinline__ uint2 pack_h(const float (&f)[Traits<T>::kVec / 2]);
+
+template <>
+__device__ __forceinline__ uint2 pack_h<float>(const float (&f)[2]) {
+  return make_uint2(__float_as_uint(f[0]), __float_as_uint(f[1]));
+}
+
+template <>
+__device__ __forceinline__ uint2 pack_h<__nv_bfloat16>(const float (&f)[4]) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]), b = __floats2bfloat162_rn(f[2], f[3]);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+}
+
+template <>
+__device__ __forceinline__ uint2 pack_h<__half>(const float (&f)[4]) {
+  __half2 a = __floats2half2_rn(f[0], f[1]), b = __floats2half2_rn(f[2], f[3]);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+}
+
 template <typename T>
 __device__ __forceinline__ uint4 pack(const float (&f)[Traits<T>::kVec]);
 
@@ -313,6 +362,32 @@ __device__ __forceinline__ void flush_partial(float (&acc)[VPT][E], float* __res
 #pragma unroll
     for (int i = 0; i < E; ++i) acc[k][i] = 0.f;
   }
+}
+
+// The same for a thread that owns H = 2, 4 or 8 consecutive columns (an 8-
+// or 16-byte slice of a 16- or 32-bit row): piece `a` covers columns
+// [a * H, a * H + H).
+template <int H>
+__device__ __forceinline__ void flush_piece(float (&acc)[H], float* __restrict__ partial,
+                                            int64_t part, int64_t hidden, int a, int npieces) {
+  static_assert(H == 2 || H == 4 || H == 8, "8- or 16-byte slices of 16- or 32-bit rows");
+  if (a < npieces) {
+    float* pr = partial + part * hidden + (int64_t)a * H;
+    uint64_t keep;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+    if constexpr (H == 2) {
+      asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;"
+                   :: "l"(pr), "f"(acc[0]), "f"(acc[1]), "l"(keep) : "memory");
+    } else {
+#pragma unroll
+      for (int i = 0; i < H; i += 4)
+        asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;"
+                     :: "l"(pr + i), "f"(acc[i]), "f"(acc[i + 1]), "f"(acc[i + 2]),
+                        "f"(acc[i + 3]), "l"(keep) : "memory");
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < H; ++i) acc[i] = 0.f;
 }
 
 // Correctly rounded 1/sqrt(v).

@@ -39,6 +39,7 @@
 // and the CTA drains: the producer waits (again bounded) for each bulk copy
 // it issued before it exits.  rms_norm_wait_timeouts() reports the count.
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "cluster.cuh"
@@ -490,6 +491,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
 }
 
 
+// A thread's slice of a row: 8 bytes (HALF) or a 16-byte vector.
+template <typename T, bool HALF, typename V>
+__device__ __forceinline__ void unpack_s(const V& v, float (&f)[HALF ? Traits<T>::kVec / 2
+                                                                  : Traits<T>::kVec]) {
+  if constexpr (HALF)
+    unpack_h<T>(v, f);
+  else
+    unpack<T>(v, f);
+}
+
+template <typename T, bool HALF>
+__device__ __forceinline__ void store_s(T* p, const float (&f)[HALF ? Traits<T>::kVec / 2
+                                                                   : Traits<T>::kVec]) {
+  if constexpr (HALF)
+    *reinterpret_cast<uint2*>(p) = pack_h<T>(f);
+  else
+    st_vec(p, pack<T>(f));
+}
+
 // Backward for narrow rows, in stages of K consecutive rows (produce_rows).
 // One row a stage leaves such rows paced by handshakes rather than by
 // bandwidth: every row cost the producer an mbarrier arm and two bulk
@@ -504,9 +524,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
 // meets a stage again only at its own row K * stages later.  The appliers
 // (one 16-byte vector of every row a thread) walk the stage's rows in order,
 // so every dw accumulator still adds its rows in row order and the results
-// are bit for bit those of bwd_tma.  Blocks of rows (RowBlocks) are whole
-// stages: K divides brows.
-template <typename T, int K>
+// are bit for bit those of bwd_tma.  An applier owns an 8-byte slice of
+// every row (HALF: twice the threads of 16-byte vectors, each with half the
+// arithmetic a row; measured faster for rows up to 2 KB, slower for 4 KB
+// rows) or a 16-byte vector.  Blocks of rows (RowBlocks) are whole stages:
+// K divides brows.
+template <typename T, int K, bool HALF>
 __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma_rows(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
     const float* __restrict__ rstd, T* __restrict__ dx, float* __restrict__ partial,
@@ -595,15 +618,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma_rows(
     return;
   }
 
+  // an applier's slice of a row: H columns in one V
+  constexpr int H = HALF ? E / 2 : E;
+  using V = std::conditional_t<HALF, uint2, uint4>;
+  const int npieces = hidden / H;
   const int a = threadIdx.x - 32 * (1 + reducers);
-  float ge[E], acc[1][E];
+  float ge[H], acc[H];
   {
-    const uint4 q = a < nvec ? ld_shared_ro(gamma + (int64_t)a * E) : make_uint4(0, 0, 0, 0);
-    unpack<T>(q, ge);
+    const V q = a < npieces ? __ldg(reinterpret_cast<const V*>(gamma) + a) : V{};
+    unpack_s<T, HALF>(q, ge);
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
+    for (int e = 0; e < H; ++e) {
       ge[e] += off;
-      acc[0][e] = 0.f;
+      acc[e] = 0.f;
     }
   }
   RingPos pos{0, 0u};
@@ -614,21 +641,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma_rows(
     bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
     ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
     if (!__all_sync(0xffffffffu, ok)) return;
-    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)pos.stage * stride);
+    const V* st = reinterpret_cast<const V*>(ring + (size_t)pos.stage * stride);
 #pragma unroll
     for (int r = 0; r < K; ++r) {
-      if (r < k && a < nvec) {
+      if (r < k && a < npieces) {
         const float c = cst[pos.stage * K + r], rs = rst[pos.stage * K + r];
-        float xf[E], df[E], o[E];
-        unpack<T>(st[r * nvec + a], xf);
-        unpack<T>(st[(K + r) * nvec + a], df);
+        float xf[H], df[H], o[H];
+        unpack_s<T, HALF>(st[r * npieces + a], xf);
+        unpack_s<T, HALF>(st[(K + r) * npieces + a], df);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
+        for (int e = 0; e < H; ++e) {
           const float xh = xf[e] * rs;
-          acc[0][e] = fmaf(df[e], xh, acc[0][e]);
+          acc[e] = fmaf(df[e], xh, acc[e]);
           o[e] = fmaf(-xh, c, df[e] * ge[e]) * rs;
         }
-        st_vec(dx + rw.row(i + r) * hidden + (int64_t)a * E, pack<T>(o));
+        store_s<T, HALF>(dx + rw.row(i + r) * hidden + (int64_t)a * H, o);
       }
     }
     i += k;
@@ -636,7 +663,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma_rows(
     if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
     pos.advance(1, stages);
     if (i == bend) {
-      flush_partial<1, E>(acc, partial, part, hidden, 0, a, appliers, nvec);
+      flush_piece<H>(acc, partial, part, hidden, a, npieces);
       ++part;
       bend = blk.block_end(i);
     }
@@ -1478,19 +1505,20 @@ int rows_per_stage(int64_t row_bytes, int64_t block_rows) {
   return k;
 }
 
-template <typename T, int K>
+template <typename T, int K, bool HALF>
 bool try_bwd_rows_k(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
   const int stride = (2 * K * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   const int gain_bytes = (a.hidden * 4 + 127) / 128 * 128;
   int stages = 0, reducers = 0;
   split_stages((kRingBudget - gain_bytes) / stride, &stages, &reducers);
-  const int appliers = ((int)(a.hidden / E) + 31) / 32 * 32;
+  // a slice of every row an applier (bwd_tma_rows)
+  const int appliers = ((int)(a.hidden / (HALF ? E / 2 : E)) + 31) / 32 * 32;
   if (stages < 3 || appliers > kMaxThreads - 32 * (1 + reducers)) return false;
   const BlockPlan bp = bwd_plan(a, err);
   if (*err != cudaSuccess) return true;
   *nparts = bp.nblocks;
-  auto kern = bwd_tma_rows<T, K>;
+  auto kern = bwd_tma_rows<T, K, HALF>;
   if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
   *err = launch_kernel(kern, dim3(bp.units), dim3(32 * (1 + reducers) + appliers),
                        (size_t)gain_bytes + (size_t)stages * stride, s, 1,
@@ -1503,12 +1531,16 @@ bool try_bwd_rows_k(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t*
 template <typename T>
 bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
+  // 8-byte applier slices for rows up to 2 KB, 16-byte ones above
+  const bool half = a.hidden * (int64_t)sizeof(T) <= 2048;
   switch (rows_per_stage(a.hidden * (int64_t)sizeof(T), a.block_rows)) {
     case 4:
-      if (try_bwd_rows_k<T, 4>(a, s, err, nparts)) return true;
+      if (try_bwd_rows_k<T, 4, true>(a, s, err, nparts)) return true;
       break;
     case 2:
-      if (try_bwd_rows_k<T, 2>(a, s, err, nparts)) return true;
+      if (half ? try_bwd_rows_k<T, 2, true>(a, s, err, nparts)
+               : try_bwd_rows_k<T, 2, false>(a, s, err, nparts))
+        return true;
       break;
     default:
       break;
