@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
       float part[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) part[e] = 0.f;
-#pragma unroll 2
+#pragma unroll 4
       for (int v = lane; v < nvec; v += 32) {
         float xf[E], df[E], gf[E];
         unpack<T>(st[v], xf);
