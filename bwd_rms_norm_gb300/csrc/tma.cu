@@ -950,15 +950,22 @@ __global__ void __launch_bounds__(VPT == 2 ? kLnBwd2Threads : kMaxThreads, 1) ln
 // Backward for wide rows (2048 vectors: 16384 16-bit or 8192 fp32 elements)
 // that bwd_tma cannot hold: its fp32 gain copy and two ring stages would
 // fill shared memory, and two vectors per applier do not cover the row.
-// Here the reducers read the gains through L1 (16-byte loads, every row)
-// instead of a shared-memory copy, which leaves room for three stages, and
-// each applier owns four vectors with its gains kept packed in registers
+// Here the gains are staged once in their own dtype (one bulk copy, behind
+// the ring's three stages: up to kWideBudget of shared memory), and each
+// applier owns four vectors with its gains kept packed in registers
 // (widened at each use) next to its fp32 dw accumulators; the block is
 // limited to 736 threads, which leaves 88 registers a thread.  A row's dot
 // is split over a team of kWideTeam reducer warps (three teams, each taking
-// every third row) that meet at their own named barrier.
+// every third row) that meet at their own named barrier.  The row dot is
+// what paces these rows: measured on GB300, a backward whose reducers skip
+// it runs 25 % faster, one whose appliers skip theirs 10 % -- hence the
+// shared-memory gains (read through L1 every row they cost a load from L2
+// a vector).
 constexpr int kWideThreads = 736;
 constexpr int kWideTeam = 2;  // warps a reducer team (three teams)
+// Dynamic shared memory of the wide and split kernels: ring and gain copy
+// (the opt-in limit is 227 KB a block, static shared memory included).
+constexpr int kWideBudget = 225 * 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
@@ -969,14 +976,20 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
   constexpr int VPT = 4;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Pipe pipe;
+  __shared__ uint64_t gbar;  // the gain copy landed
   const int row_bytes = hidden * (int)sizeof(T);
   const int stride = (2 * row_bytes + 127) / 128 * 128;
   unsigned char* ring = smem;
+  const uint4* gsm = reinterpret_cast<const uint4*>(smem + (size_t)stages * stride);
   const int appliers = blockDim.x - 32 * (1 + reducers * kWideTeam);
   const RowBlocks blk = row_blocks(rows, brows, blockIdx.x, gridDim.x);
   const Rows rw{blk.r0, blk.n};
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
+  if (threadIdx.x == 0) {
+    mbar_init(&gbar, 1);
+    fence_mbar_init();
+  }
   __syncthreads();
   pdl_trigger();
   pdl_wait();
@@ -987,8 +1000,11 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
 
   if (warp == 0) {
     if (lane == 0) {
+      mbar_arrive_expect_tx(&gbar, (uint32_t)row_bytes);
+      bulk_load(smem + (size_t)stages * stride, gamma, (uint32_t)row_bytes, &gbar);
       const void* const src[2] = {x, dy};
       produce<2>(pipe, ring, stride, stages, src, rw, (uint32_t)row_bytes, abort);
+      drain_phase(&gbar, 0);
     }
     return;
   }
@@ -1000,10 +1016,12 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
     int tpar = 0;
     RingPos pos{0, 0u};
     pos.advance(d, stages);
+    const bool gok = d < n ? __all_sync(0xffffffffu, wait_phase(&gbar, 0, abort)) : true;
     for (int i = d; i < n; i += reducers) {
       const float rs = __ldg(rstd + rw.row(i));
       // the team decides together: a named barrier that ANDs every warp's wait
-      const bool ok = __all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort));
+      const bool ok =
+          __all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort)) && gok;
       uint32_t all_ok;
       asm volatile(
           "{\n\t.reg .pred p, q;\n\t"
@@ -1022,7 +1040,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
         float xf[E], df[E], gf[E];
         unpack<T>(st[v], xf);
         unpack<T>(st[doff + v], df);
-        unpack<T>(ld_shared_ro(gamma + (int64_t)v * E), gf);
+        unpack<T>(gsm[v], gf);
 #pragma unroll
         for (int e = 0; e < E; ++e) part[e] = fmaf(df[e] * (gf[e] + off), xf[e], part[e]);
       }
@@ -1103,14 +1121,14 @@ AttrEntry g_attr_done[128];
 int g_attr_n = 0;
 
 // Raise a kernel's dynamic shared memory limit, once per (kernel, device).
-cudaError_t allow_smem(const void* kern) {
+cudaError_t allow_smem(const void* kern, int bytes = kRingBudget) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   for (int i = 0; i < g_attr_n; ++i)
     if (g_attr_done[i].func == kern && g_attr_done[i].device == dev) return cudaSuccess;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBudget);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && g_attr_n < 128) g_attr_done[g_attr_n++] = AttrEntry{kern, dev};
   return e;
 }
@@ -1256,11 +1274,13 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
   __shared__ uint64_t xbar[3][2];
   __shared__ float xch[3][2][CS];
   __shared__ float tred[3][2][kWideTeam];
+  __shared__ uint64_t gbar;  // the gain copy landed
   const uint32_t rank = cta_rank();
   const int part = hidden / csize;           // columns a CTA owns
   const int part_bytes = part * (int)sizeof(T);
   const int stride = (2 * part_bytes + 127) / 128 * 128;
   unsigned char* ring = smem;
+  const uint4* gsm = reinterpret_cast<const uint4*>(smem + (size_t)stages * stride);
   const int appliers = blockDim.x - 32 * (1 + reducers * kWideTeam);
   const int64_t cid = blockIdx.x / csize, ncl = gridDim.x / csize;
   const RowBlocks blk = row_blocks(rows, brows, cid, ncl);
@@ -1268,6 +1288,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
   if (threadIdx.x < 6) mbar_init(&xbar[threadIdx.x / 2][threadIdx.x % 2], csize);
+  if (threadIdx.x == 6) mbar_init(&gbar, 1);
   fence_mbar_init();
   __syncthreads();
   cluster_sync();  // the peers' barriers are initialised
@@ -1281,9 +1302,12 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
 
   if (warp == 0) {
     if (lane == 0) {
+      mbar_arrive_expect_tx(&gbar, (uint32_t)part_bytes);
+      bulk_load(smem + (size_t)stages * stride, gamma + col0, (uint32_t)part_bytes, &gbar);
       const void* const src[2] = {x + col0, dy + col0};
       produce_pitched<2>(pipe, ring, stride, stages, src, rw, (size_t)hidden * sizeof(T),
                          (uint32_t)part_bytes, abort);
+      drain_phase(&gbar, 0);
     }
   } else if (warp <= reducers * kWideTeam) {
     const int d = (warp - 1) / kWideTeam, tw = (warp - 1) % kWideTeam;
@@ -1293,10 +1317,11 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
     bool prev_ok = true;  // the team's last exchange (its first warp)
     RingPos pos{0, 0u};
     pos.advance(d, stages);
+    const bool gok = d < n ? __all_sync(0xffffffffu, wait_phase(&gbar, 0, abort)) : true;
     for (int i = d; i < n; i += reducers) {
       const float rs = __ldg(rstd + rw.row(i));
       const bool ok = __all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort)) &&
-                      prev_ok;
+                      prev_ok && gok;
       uint32_t all_ok;
       asm volatile(
           "{\n\t.reg .pred p, q;\n\t"
@@ -1315,7 +1340,7 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
         float xf[E], df[E], gf[E];
         unpack<T>(st[v], xf);
         unpack<T>(st[doff + v], df);
-        unpack<T>(ld_shared_ro(gamma + col0 + (int64_t)v * E), gf);
+        unpack<T>(gsm[v], gf);
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[e] = fmaf(df[e] * (gf[e] + off), xf[e], acc[e]);
       }
@@ -1423,7 +1448,8 @@ bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t
   for (int k = 2; k <= kMaxSplit; k *= 2) {
     if (a.hidden % (k * E)) continue;
     const int stride = (2 * (a.hidden / k) * (int)sizeof(T) + 127) / 128 * 128;
-    int st = kRingBudget / stride;
+    const int gain = ((a.hidden / k) * (int)sizeof(T) + 127) / 128 * 128;
+    int st = (kWideBudget - gain) / stride;
     if (st > kMaxStages) st = kMaxStages;
     st -= st % reducers;
     // four vectors an applier (the kernel's packed gains)
@@ -1436,14 +1462,15 @@ bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t
   }
   if (csize == 0) return false;
   const int stride = (2 * (a.hidden / csize) * (int)sizeof(T) + 127) / 128 * 128;
+  const int gain = ((a.hidden / csize) * (int)sizeof(T) + 127) / 128 * 128;
   const int threads = 32 * (1 + reducers * kWideTeam) + appliers;
   auto kern = csize == 2 ? bwd_tma_split<T, 2> : bwd_tma_split<T, 4>;
-  if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
+  if ((*err = allow_smem((const void*)kern, kWideBudget)) != cudaSuccess) return true;
   // as many clusters as can be resident at once (one CTA per SM)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)csize);
   cfg.blockDim = dim3((unsigned)threads);
-  cfg.dynamicSmemBytes = (size_t)stages * stride;
+  cfg.dynamicSmemBytes = (size_t)stages * stride + gain;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)csize;
@@ -1464,7 +1491,7 @@ bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t
   const BlockPlan bp = plan_blocks(a.rows, a.block_rows, unit_cap(a, active));
   *nparts = bp.nblocks;
   *err = launch_kernel(kern, dim3((unsigned)(csize * bp.units)), dim3(threads),
-                       (size_t)stages * stride, s, csize, static_cast<const T*>(a.dy),
+                       (size_t)stages * stride + gain, s, csize, static_cast<const T*>(a.dy),
                        static_cast<const T*>(a.x), static_cast<const T*>(a.gamma), a.rstd,
                        static_cast<T*>(a.dx), a.partial, a.rows, a.hidden,
                        a.offset ? 1.f : 0.f, stages, reducers, bp.brows);
@@ -1478,7 +1505,8 @@ template <typename T>
 bool try_bwd_wide_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
   const int stride = (2 * a.hidden * (int)sizeof(T) + 127) / 128 * 128;
-  const int stages = kRingBudget / stride >= 3 ? 3 : 0, reducers = 3;
+  const int gain = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
+  const int stages = 3 * stride + gain <= kWideBudget ? 3 : 0, reducers = 3;
   if (stages < 3) return false;
   int appliers = 0;
   if (pick_vpt(a.hidden / E, kWideThreads - 32 * (1 + reducers * kWideTeam), 4, &appliers) != 4)
@@ -1487,9 +1515,9 @@ bool try_bwd_wide_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t*
   if (*err != cudaSuccess) return true;
   *nparts = bp.nblocks;
   auto kern = bwd_tma_wide<T>;
-  if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
+  if ((*err = allow_smem((const void*)kern, kWideBudget)) != cudaSuccess) return true;
   *err = launch_kernel(kern, dim3(bp.units), dim3(32 * (1 + reducers * kWideTeam) + appliers),
-                       (size_t)stages * stride, s, 1, static_cast<const T*>(a.dy),
+                       (size_t)stages * stride + gain, s, 1, static_cast<const T*>(a.dy),
                        static_cast<const T*>(a.x), static_cast<const T*>(a.gamma), a.rstd,
                        static_cast<T*>(a.dx), a.partial, a.rows, a.hidden,
                        a.offset ? 1.f : 0.f, stages, reducers, bp.brows);
