@@ -846,7 +846,7 @@ __global__ void __launch_bounds__(VPT == 2 ? kLnBwd2Threads : kMaxThreads, 1) ln
       float p1[E], p2[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) p1[e] = p2[e] = 0.f;
-#pragma unroll 2
+#pragma unroll(VPT == 2 ? 4 : 2)
       for (int v = lane; v < nvec; v += 32) {
         float xf[E], df[E], gf[E];
         unpack<T>(st[v], xf);
@@ -1434,16 +1434,15 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
 // The split backward: clusters of csize CTAs, the smallest csize (2 or 4)
 // whose parts of a row leave at least min_stages ring stages (a multiple of
 // the three reducer teams), else the largest that leaves three.  Measured
-// on GB300: fp32 rows gain from six stages (16384 fp32: 0.78 of the copy
-// bandwidth in clusters of 4 against 0.69 in pairs), 16-bit rows do not
-// (32768 fp16: 0.64 in pairs with three stages, 0.62 in clusters of 4 with
-// six), having twice the arithmetic per staged byte.  False when none fits.
+// on GB300: six stages beat three (16384 fp32: 0.78 of the copy bandwidth
+// in clusters of 4 against 0.69 in pairs; 32768 fp16, gains in shared
+// memory: 158.7 against 164.1 us).  False when none fits.
 
 template <typename T>
 bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* nparts) {
   constexpr int E = Traits<T>::kVec;
   const int reducers = 3;
-  const int min_stages = sizeof(T) == 4 ? 6 : 3;
+  const int min_stages = 6;
   int csize = 0, stages = 0, appliers = 0;
   for (int k = 2; k <= kMaxSplit; k *= 2) {
     if (a.hidden % (k * E)) continue;
