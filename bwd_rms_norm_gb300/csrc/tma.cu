@@ -1203,17 +1203,21 @@ cudaError_t launch_fwd_tma_v(const FwdArgs& a, int appliers, int stages, int red
 }
 
 template <typename T>
+bool try_fwd_split_t(const FwdArgs& a, cudaStream_t s, cudaError_t* err);
+
+template <typename T>
 bool try_fwd_tma_t(const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
   constexpr int E = Traits<T>::kVec;
   const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   int stages = 0, reducers = 0;
   split_stages((stride <= 16 * 1024 ? kFwdRingBytes : kRingBudget) / stride, &stages,
                &reducers);
-  if (stages < 3) return false;
+  // rows too wide for this kernel go over a cluster (fwd_tma_split)
+  if (stages < 3) return try_fwd_split_t<T>(a, s, err);
   int appliers = 0;
   // at most 4 vectors per applier (gains in fp32 registers)
   const int vpt = pick_vpt(a.hidden / E, kMaxThreads - 32 * (1 + reducers), 4, &appliers);
-  if (vpt == 0) return false;
+  if (vpt == 0) return try_fwd_split_t<T>(a, s, err);
   const int grid = grid_for(a.rows, a.rows, err);
   if (*err != cudaSuccess) return true;
   switch (vpt) {
@@ -1497,7 +1501,244 @@ bool try_bwd_split_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t
   return true;
 }
 
-// The wide-row backward: three stages without a shared gain copy and four
+// Forward for rows too wide for fwd_tma (its appliers would need more than
+// four vectors each, or its ring would hold fewer than three rows): a row is
+// split over a cluster of CS (2 or 4) CTAs as in bwd_tma_split -- CTA q
+// stages columns [q * N/CS, (q + 1) * N/CS) of every row of the cluster's
+// contiguous rows -- so that a stage is small enough for six or more.
+// Reducer warp d takes the cluster's rows d, d + R, ...: the sum of squares
+// of its slice (as fwd_tma's reducers), sent to every CTA of the cluster
+// through distributed shared memory (slot `rank` of the warp's buffer, two
+// buffers used in turn, each with an mbarrier that counts the CS arrivals),
+// then the CS parts added in rank order, so that every CTA holds the same
+// rstd.  A row whose fp32 total overflows takes a second exchange, of the
+// rescaled sums (every CTA sees the same total, so all of them take it).
+// The double buffer is safe for the same reason as bwd_tma_split's: a CTA
+// sends its part of exchange e + 1 only after reading exchange e, so no
+// part of exchange e + 2 lands before every CTA has read exchange e.  The
+// appliers are fwd_tma's on the CTA's columns, with the gains packed in
+// registers.  No role leaves early: every CTA ends at a cluster barrier,
+// so that none exits while a peer may still store into its shared memory.
+template <int CS>
+__device__ __forceinline__ bool exchange_sum(float mine, float (&slot)[CS], uint64_t* bar,
+                                             uint32_t& phase, uint32_t rank, int lane,
+                                             volatile int* abort, float* total) {
+  if (lane < CS) {
+    st_peer(&slot[rank], (uint32_t)lane, mine);
+    mbar_arrive_peer(bar, (uint32_t)lane);
+  }
+  if (!__all_sync(0xffffffffu, wait_cluster_counted(bar, phase, abort, &g_wait_timeouts)))
+    return false;
+  phase ^= 1u;
+  float t = 0.f;
+#pragma unroll
+  for (int r = 0; r < CS; ++r) t += slot[r];
+  *total = t;
+  return true;
+}
+
+template <typename T, int CS, bool F8>
+__global__ void __launch_bounds__(kWideThreads, 1) fwd_tma_split(
+    const T* __restrict__ x, const T* __restrict__ gamma, void* __restrict__ y,
+    float* __restrict__ rstd, int64_t rows, int hidden, float eps, float off, int twice,
+    const float* __restrict__ scale, int stages, int reducers) {
+  constexpr int E = Traits<T>::kVec;
+  constexpr int VPT = 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Pipe pipe;
+  __shared__ uint64_t xbar[kMaxReducers][2];
+  __shared__ float xch[kMaxReducers][2][CS];
+  const uint32_t rank = cta_rank();
+  const int part = hidden / CS;  // columns a CTA owns
+  const int part_bytes = part * (int)sizeof(T);
+  const int stride = (part_bytes + 127) / 128 * 128;
+  const int appliers = blockDim.x - 32 * (1 + reducers);
+  const int64_t cid = blockIdx.x / CS, ncl = gridDim.x / CS;
+  const int64_t r0 = cid * rows / ncl;
+  const Rows rw{r0, (int)((cid + 1) * rows / ncl - r0)};
+  const int n = rw.n;
+  init_pipe(pipe, stages, appliers / 32);
+  if (threadIdx.x < 2 * kMaxReducers) mbar_init(&xbar[threadIdx.x / 2][threadIdx.x % 2], CS);
+  fence_mbar_init();
+  __syncthreads();
+  cluster_sync();  // the peers' barriers are initialised
+  pdl_trigger();
+  pdl_wait();
+  volatile int* abort = &pipe.abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = part / E;                  // vectors of this CTA's columns
+  const int64_t col0 = (int64_t)rank * part;  // first column of this CTA
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const void* const src[1] = {x + col0};
+      produce_pitched<1>(pipe, smem, stride, stages, src, rw, (size_t)hidden * sizeof(T),
+                         (uint32_t)part_bytes, abort);
+    }
+  } else if (warp <= reducers) {
+    const int d = warp - 1;
+    int par = 0;
+    uint32_t ph[2] = {0u, 0u};
+    RingPos pos{0, 0u};
+    pos.advance(d, stages);
+    for (int i = d; i < n; i += reducers) {
+      if (!__all_sync(0xffffffffu, wait_phase(&pipe.full[pos.stage], pos.phase, abort))) break;
+      const uint4* st = reinterpret_cast<const uint4*>(smem + (size_t)pos.stage * stride);
+      float acc[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
+        float f[E];
+        unpack<T>(st[v], f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(f[e], f[e], acc[e]);
+      }
+      float ss;
+      if (!exchange_sum<CS>(warp_sum(pairwise<E>(acc)), xch[d][par], &xbar[d][par], ph[par], rank,
+                            lane, abort, &ss))
+        break;
+      par ^= 1;
+      float rs = rstd_of(ss / (float)hidden, eps);
+      if (isinf(ss)) {  // the fp32 sum of squares overflowed (see kOverflowScale)
+        float s2 = 0.f;
+        for (int v = lane; v < nvec; v += 32) {
+          float f[E];
+          unpack<T>(st[v], f);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float t = f[e] * kOverflowScale;
+            s2 = fmaf(t, t, s2);
+          }
+        }
+        float tot;
+        if (!exchange_sum<CS>(warp_sum(s2), xch[d][par], &xbar[d][par], ph[par], rank, lane,
+                              abort, &tot))
+          break;
+        par ^= 1;
+        rs = rstd_rescaled(tot, hidden, eps);
+      }
+      if (lane == 0) {
+        if (rank == 0) rstd[rw.row(i)] = rs;
+        pipe.stat[pos.stage] = rs;
+        mbar_arrive(&pipe.red[pos.stage]);
+        mbar_arrive(&pipe.empty[pos.stage]);
+      }
+      pos.advance(reducers, stages);
+    }
+  } else {
+    const int a = threadIdx.x - 32 * (1 + reducers);
+    const float sc = F8 ? __ldg(scale) : 1.f;
+    uint4 gp[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int v = a + j * appliers;
+      gp[j] = v < nvec ? ld_shared_ro(gamma + col0 + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
+    }
+    RingPos pos{0, 0u};
+    for (int i = 0; i < n; ++i) {
+      bool ok = wait_phase(&pipe.red[pos.stage], pos.phase, abort);
+      ok = ok && wait_phase(&pipe.full[pos.stage], pos.phase, abort);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const float rs = pipe.stat[pos.stage];
+      const uint4* st = reinterpret_cast<const uint4*>(smem + (size_t)pos.stage * stride);
+      const int64_t yoff = rw.row(i) * hidden + col0;
+      // widen the packed gains at each use rather than holding them widened
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) opaque(gp[j]);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j) {
+        const int v = a + j * appliers;
+        if (v < nvec) {
+          float f[E], g[E], o[E];
+          unpack<T>(st[v], f);
+          unpack<T>(gp[j], g);
+          if constexpr (F8) {
+            // ((x * rstd) * gain) * scale in fp32, one conversion to E4M3
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] = ((f[e] * rs) * (g[e] + off)) * sc;
+            st_e4m3<E>(static_cast<unsigned char*>(y) + yoff + (int64_t)v * E, o);
+          } else {
+            if (twice) {
+#pragma unroll
+              for (int e = 0; e < E; ++e) o[e] = round_trip<T>(f[e] * rs) * (g[e] + off);
+            } else {
+#pragma unroll
+              for (int e = 0; e < E; ++e) o[e] = (f[e] * rs) * (g[e] + off);
+            }
+            st_vec(static_cast<T*>(y) + yoff + (int64_t)v * E, pack<T>(o));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pipe.empty[pos.stage]);
+      pos.advance(1, stages);
+    }
+  }
+  __syncwarp();
+  cluster_sync();  // no peer stores into this CTA after it exits
+}
+
+// The split forward: clusters of CS CTAs, the smallest CS (2 or 4) whose
+// parts of a row leave at least six ring stages, else the largest that
+// leaves three, with four vectors an applier; false when none fits.
+template <typename T, bool F8>
+bool try_fwd_split_tf(const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
+  constexpr int E = Traits<T>::kVec;
+  int csize = 0, stages = 0, reducers = 0, appliers = 0;
+  for (int k = 2; k <= kMaxSplit; k *= 2) {
+    if (a.hidden % (k * E)) continue;
+    const int stride = ((int)(a.hidden / k) * (int)sizeof(T) + 127) / 128 * 128;
+    int st = 0, r = 0;
+    split_stages(kRingBudget / stride, &st, &r);
+    const int app = ((int)(a.hidden / k / E + 3) / 4 + 31) / 32 * 32;
+    if (st < 3 || app > kWideThreads - 32 * (1 + r)) continue;
+    csize = k;
+    stages = st;
+    reducers = r;
+    appliers = app;
+    if (st >= 6) break;
+  }
+  if (csize == 0) return false;
+  const int stride = ((int)(a.hidden / csize) * (int)sizeof(T) + 127) / 128 * 128;
+  const int threads = 32 * (1 + reducers) + appliers;
+  auto kern = csize == 2 ? fwd_tma_split<T, 2, F8> : fwd_tma_split<T, 4, F8>;
+  if ((*err = allow_smem((const void*)kern)) != cudaSuccess) return true;
+  // as many clusters as can be resident at once (one CTA per SM)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)csize);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)stages * stride;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int active = 0;
+  if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) {
+    cudaGetLastError();
+    return false;
+  }
+  int dev = 0;
+  if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return true;
+  const int budget = sm_count(dev) / csize;  // the SM budget, in clusters
+  if (active > budget) active = budget > 0 ? budget : 1;
+  const int64_t clusters = a.rows < active ? a.rows : active;
+  *err = launch_kernel(kern, dim3((unsigned)(csize * clusters)), dim3(threads),
+                       (size_t)stages * stride, s, csize, static_cast<const T*>(a.x),
+                       static_cast<const T*>(a.gamma), a.y, a.rstd, a.rows, a.hidden, a.eps,
+                       a.offset ? 1.f : 0.f, a.twice, a.scale, stages, reducers);
+  return true;
+}
+
+template <typename T>
+bool try_fwd_split_t(const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
+  return a.fp8 ? try_fwd_split_tf<T, true>(a, s, err) : try_fwd_split_tf<T, false>(a, s, err);
+}
+
+// The wide-row backward: three stages with a packed gain copy and four
 // vectors per applier within kWideThreads threads; false when that does not
 // fit either.
 template <typename T>

@@ -41,7 +41,7 @@ RMS = [
     ("fp16_4096x2048", "fwd_cta_row", "bwd_tma_rowsI6__halfLi2E"),
     ("fp16_4096x8192", "fwd_tma", "7bwd_tmaI"),
     ("fp16_4096x16384", "fwd_tma", "bwd_tma_wide"),
-    ("fp16_4096x32768", "fwd_cta_row", "bwd_tma_split"),
+    ("fp16_4096x32768", "fwd_tma_split", "bwd_tma_split"),
     ("large_bf16_16384x8192_once", "fwd_tma", "7bwd_tmaI"),
     ("fp32_256x1024", "fwd_cta_row", "bwd_tma_rowsIfLi2E"),
 ]

@@ -65,7 +65,7 @@ def test_named_fp8_workload(L, name):
 SHAPES = [(1, 1, "f32"), (3, 8, "bf16"), (17, 24, "f16"), (5, 1001, "bf16"), (9, 1024, "bf16"),
           (7, 1032, "f16"), (300, 4096, "bf16"), (40, 3072, "f32"), (4, 16384, "bf16"),
           (3, 16392, "f16"), (2, 32768, "f32"), (2, 65536, "bf16"), (2, 65536, "f32"),
-          (611, 12288, "bf16"), (1000, 8192, "f16")]
+          (611, 12288, "bf16"), (1000, 8192, "f16"), (40, 32768, "bf16"), (9, 16384, "f32")]
 
 
 @pytest.mark.parametrize("rows,hidden,dtype", SHAPES)

@@ -96,7 +96,8 @@ def test_fp16_overflow_stress(L):
 
 @pytest.mark.parametrize("rows,hidden,dtype", [
     (64, 1024, "bf16"), (40, 2048, "f32"), (24, 4096, "bf16"), (16, 8192, "f32"),
-    (12, 16384, "bf16"), (6, 65536, "f32"), (10, 1001, "bf16"), (8, 3, "f32")])
+    (12, 16384, "bf16"), (6, 65536, "f32"), (10, 1001, "bf16"), (8, 3, "f32"),
+    (8, 32768, "bf16"), (6, 16384, "f32")])
 def test_sum_of_squares_past_fp32(L, rows, hidden, dtype):
     """Rows of bf16/fp32 values so large that an fp32 sum of squares
     overflows (every square past 2**128 for the 2**70 rows; only the sum for
@@ -124,12 +125,14 @@ SHAPES = [
     (3, 16392, "bf16"), (2, 32768, "f32"), (2, 65536, "bf16"), (2, 65536, "f32"),
     (2, 65536, "f16"), (300, 4096, "bf16"), (151, 2048, "f16"), (153, 512, "f32"),
     (1, 32768, "f16"), (33, 3072, "bf16"), (2, 7, "f16"),
-    # the staged backward for 2048-vector rows (gains read through L1, four
-    # vectors per applier): ragged row counts over the 152-CTA grid
+    # the staged backward for 2048-vector rows (a packed gain copy in shared
+    # memory, four vectors per applier): ragged row counts over the 152-CTA
+    # grid
     (1000, 16384, "f16"), (157, 16384, "bf16"), (301, 8192, "f32"),
-    # the paired-CTA backward for 4096-vector rows (each CTA of a cluster of
-    # two stages half of every row): ragged row counts over the pairs, fewer
-    # rows than pairs, and a width between 2048 and 4096 vectors
+    # the cluster-split forward and backward for 4096-vector rows (each CTA
+    # of a cluster stages its part of every row): ragged row counts over the
+    # clusters, fewer rows than clusters, and a width between 2048 and 4096
+    # vectors
     (300, 32768, "f16"), (157, 16384, "f32"), (5, 32768, "bf16"), (77, 24576, "bf16"),
 ]
 
@@ -151,6 +154,22 @@ def test_modes(L, dtype, offset, cast_mode, hidden):
     w = W.Workload("modes", 64, hidden, dtype, 1e-6, offset, cast_mode,
                    ("normal", 0.0, 2.0), gamma_dist, ("normal", 0.0, 1.0), seed=11)
     run_and_check(L, w)
+
+
+@pytest.mark.parametrize("rows,hidden,dtype", [(40, 32768, "bf16"), (33, 32768, "f16"),
+                                               (20, 16384, "f32")])
+@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("cast_mode", ["round_once", "round_twice"])
+def test_split_forward_modes(L, rows, hidden, dtype, offset, cast_mode):
+    """Rows split over a cluster in the forward (fwd_tma_split): both cast
+    modes and the Gemma offset, against the oracle."""
+    gamma_dist = ("normal", 0.0, 0.1) if offset else ("uniform", 0.9, 1.1)
+    w = W.Workload("split_modes", rows, hidden, dtype, 1e-6, offset, cast_mode,
+                   ("normal", 0.0, 2.0), gamma_dist, ("normal", 0.0, 1.0), seed=rows + offset)
+    inp = W.make_inputs(w)
+    L.rms_norm_fwd(inp["x"].cuda(), inp["gamma"].cuda(), w.eps, w.offset, w.cast_mode)
+    assert any("fwd_tma_split" in k for k in L.last_kernels()), L.last_kernels()
+    run_and_check(L, w, inputs=inp)
 
 
 def _misaligned_copy(t: torch.Tensor, shift_elems: int = 1) -> torch.Tensor:
