@@ -20,9 +20,16 @@
 //       c = sum(g * x_hat) / hidden in the backward -- into the stage's slot;
 //                                                                 -> red[s]
 //   appliers (the remaining threads)  walk every row in order; each thread
-//       owns the same 16-byte vectors of every row, keeps their fp32 gains
-//       (and in the backward their fp32 dw accumulators) in registers, and
-//       writes y or dx with 128-bit stores.  No barrier among the appliers.
+//       owns the same 16-byte vectors of every row (8-byte slices in the
+//       narrow-row backward), keeps their gains (and in the backward their
+//       fp32 dw accumulators) in registers, and writes y or dx with 128-bit
+//       stores.  No barrier among the appliers.
+//
+// Narrow rows (up to 4 KB) are staged several to a stage in the backward
+// (bwd_tma_rows), so that a stage's handshakes serve several rows; rows too
+// wide for one CTA's ring are split over a cluster (fwd_tma_split,
+// bwd_tma_split), and the widest single-CTA backward (bwd_tma_wide) keeps a
+// packed copy of the gains beside its ring.
 //
 // A stage is released (empty[s]) when its reducer and every applier warp
 // have read it.  The stage count is a multiple of R, so reducer d only ever
