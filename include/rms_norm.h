@@ -111,13 +111,14 @@ size_t rms_norm_bwd_workspace_size(int64_t rows, int64_t hidden, int dtype);
  * rms_norm_bwd_workspace_size(rows, hidden, dtype) bytes, 16-byte aligned;
  * its contents need no initialisation and are clobbered.  dw is reduced in a
  * fixed order from fp32 partials over blocks of rows, one block per CTA of
- * the launch (the rows split evenly over the CTAs, whose count the GPU's SM
- * count and the SM budget set): partial b goes to lane b mod 16, each lane
- * adds its partials in increasing b, and the 16 lane sums are added in
- * order.  Repeated calls with the same sizes and SM budget therefore give
- * bit-identical results.  rms_norm_bwd_blocked takes the
- * block size from the caller instead, for results that do not depend on the
- * GPU or on how the rows are split.  rows == 0 zero-fills dw and returns
+ * the launch, or per cluster of CTAs for rows split over a cluster (the rows
+ * split evenly over them, whose count the row width, the GPU's SM count and
+ * the SM budget set; within a block the rows are added in row order):
+ * partial b goes to lane b mod 16, each lane adds its partials in
+ * increasing b, and the 16 lane sums are added in order.  Repeated calls
+ * with the same sizes and SM budget therefore give bit-identical results.
+ * rms_norm_bwd_blocked takes the block size from the caller instead, for
+ * results that do not depend on the GPU or on how the rows are split.  rows == 0 zero-fills dw and returns
  * RMSN_OK (dy, x, rstd, dx, workspace may then be NULL).  Outputs must not
  * overlap inputs.
  */
