@@ -75,6 +75,7 @@ EXPORTED = (
     "rms_norm_set_sm_budget",
     "rms_norm_sm_budget",
     "rms_norm_wait_timeouts",
+    "rms_norm_selftest_wait_limit",
     "rms_norm_fwd_fp8",
     "layer_norm_fwd",
     "layer_norm_bwd_workspace_size",
@@ -140,6 +141,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.rms_norm_sm_budget.restype = I
     lib.rms_norm_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.rms_norm_wait_timeouts.restype = I
+    lib.rms_norm_selftest_wait_limit.argtypes = [ctypes.POINTER(ctypes.c_uint),
+                                                 ctypes.POINTER(ctypes.c_double)]
+    lib.rms_norm_selftest_wait_limit.restype = I
     lib.rms_norm_fwd_fp8.argtypes = [P, P, P, P, P, I64, I64, F, I, I, P]
     lib.rms_norm_fwd_fp8.restype = I
     lib.group_norm_fwd.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, F, I, P]
@@ -193,6 +197,16 @@ def wait_timeouts() -> int:
     if st != RMSN_OK:
         raise RMSNormError("rms_norm_wait_timeouts", st)
     return int(n.value)
+
+
+def selftest_wait_limit() -> Tuple[int, float]:
+    """Run the bounded-wait self-test (a wait on a barrier nothing completes
+    runs out after about a second): returns (waits that ran out, seconds)."""
+    n, t = ctypes.c_uint(0), ctypes.c_double(0.0)
+    st = load_library().rms_norm_selftest_wait_limit(ctypes.byref(n), ctypes.byref(t))
+    if st != RMSN_OK:
+        raise RMSNormError("rms_norm_selftest_wait_limit", st)
+    return int(n.value), float(t.value)
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:

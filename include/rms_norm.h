@@ -352,6 +352,17 @@ int rms_norm_last_launch_count(void);
  * loaded (0 in correct operation).  Synchronises with the device. */
 int rms_norm_wait_timeouts(unsigned int* count);
 
+/* Self-test of those bounded waits (both arguments are host pointers):
+ * launches one thread that waits on a shared-memory barrier nothing
+ * completes, through the same bounded wait the staged kernels use.  The
+ * wait runs out after its limit, counts in a device counter of its own (not
+ * the one rms_norm_wait_timeouts reads) and the kernel returns, leaving the
+ * context usable.  Writes that count to *timeouts (1 expected) and the
+ * seconds the call took, measured on the host, to *seconds (about one).
+ * Synchronises with the device; RMSN_ERR_NULL for a NULL argument,
+ * RMSN_ERR_CUDA if the launch or a copy fails. */
+int rms_norm_selftest_wait_limit(unsigned int* timeouts, double* seconds);
+
 /*
  * Backward without caller-provided scratch.  The method's pages describe no
  * such call; it exists for callers that cannot allocate device memory at the

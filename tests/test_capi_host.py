@@ -229,6 +229,12 @@ def test_last_kernels_without_launches(lib):
     assert lib.rms_norm_last_kernels(None, 4) < 0
 
 
+def test_selftest_rejects_null_pointers(lib):
+    n, t = ctypes.c_uint(0), ctypes.c_double(0.0)
+    assert lib.rms_norm_selftest_wait_limit(None, ctypes.byref(t)) == 1   # RMSN_ERR_NULL
+    assert lib.rms_norm_selftest_wait_limit(ctypes.byref(n), None) == 1
+
+
 def test_rms_norm_module_host_side():
     """The autograd layer builds its weight on the host, checks its
     arguments, and refuses CPU inputs like every other call."""
