@@ -529,13 +529,12 @@ __device__ __forceinline__ void store_s(T* p, const float (&f)[HALF ? Traits<T>:
 // all K have (a last stage with fewer rows gets an arrival for each missing
 // row too, after its copy landed).  R divides the stage count, so reducer d
 // meets a stage again only at its own row K * stages later.  The appliers
-// (one 16-byte vector of every row a thread) walk the stage's rows in order,
-// so every dw accumulator still adds its rows in row order and the results
-// are bit for bit those of bwd_tma.  An applier owns an 8-byte slice of
-// every row (HALF: twice the threads of 16-byte vectors, each with half the
-// arithmetic a row; measured faster for rows up to 2 KB, slower for 4 KB
-// rows) or a 16-byte vector.  Blocks of rows (RowBlocks) are whole stages:
-// K divides brows.
+// walk the stage's rows in order, so every dw accumulator still adds its
+// rows in row order and the results are bit for bit those of bwd_tma.  An
+// applier owns an 8-byte slice of every row (HALF: twice the threads of
+// 16-byte vectors, each with half the arithmetic a row; measured faster for
+// rows up to 2 KB, slower for 4 KB rows) or a 16-byte vector.  Blocks of
+// rows (RowBlocks) are whole stages: K divides brows.
 template <typename T, int K, bool HALF>
 __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma_rows(
     const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ gamma,
