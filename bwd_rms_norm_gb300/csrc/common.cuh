@@ -282,6 +282,21 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red, int 
 // are visible, so a kernel calls it before its first global memory access.
 // pdl_trigger() lets the next kernel on the stream be scheduled; it only
 // runs its own prologue before its own pdl_wait().
+// A hint to bring [p, p + bytes) into L2 (p 16-byte aligned, bytes a
+// multiple of 16); it changes no value any load returns.  The kernels issue
+// it for their first rows before griddepcontrol.wait: launched
+// programmatically, a CTA that starts while the previous kernel finishes
+// then finds its first rows in L2 when the wait ends, instead of fetching
+// them from DRAM behind every other SM's first fetch.  Measured on GB300
+// (steps of forward + backward): 16384 x 8192 bf16 6502 -> 6596 GB/s
+// (backward 121.3 -> 119.3 us), 4096 x 4096 bf16 4911 -> 5107 GB/s
+// (backward 19.59 -> 18.60 us), 4096 x 1024 fp16 backward 9.10 -> 8.01 us;
+// calls made alone unchanged.  Slower, and so left out: the LayerNorm
+// forward, the wide and the split backward.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

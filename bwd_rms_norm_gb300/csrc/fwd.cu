@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(256, 5) fwd_warp_rows(
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_trigger();
   if (row >= rows) return;  // whole warps leave together
+  if (lane == 0) prefetch_l2(x + row * hidden, (uint32_t)(hidden * sizeof(T)));
   pdl_wait();
   const int nvec = hidden / E;
   const T* xr = x + row * hidden;
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : VPT >= 4 ? 1024 : 128, VPT <=
   const int nvec = hidden / E;
   const T* xr = x + row * hidden;
   pdl_trigger();
+  if (threadIdx.x == 0) prefetch_l2(xr, (uint32_t)(hidden * sizeof(T)));
   pdl_wait();
   const float sc = F8 ? __ldg(scale) : 1.f;
 

@@ -65,6 +65,11 @@ constexpr int kMaxThreads = 1024;
 constexpr int kMaxReducers = 12;
 // Dynamic shared memory for the ring (and the backward's fp32 gain row).
 constexpr int kRingBudget = 200 * 1024;
+// Rows (stages, for the narrow-row backward) a CTA prefetches into L2
+// before its griddepcontrol.wait (see prefetch_l2): measured on GB300, four
+// beat two and a whole ring -- a whole ring's prefetches delayed the first
+// loads of a call made alone (4096 x 4096 backward alone 27.6 -> 28.7 us).
+constexpr int kPrefetchRows = 4;
 
 // Bounded waits counted in this file's timeout counter.
 __device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -257,6 +262,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
   pdl_trigger();
+  if (threadIdx.x == 0 && n > 0)  // the first rows into L2 (prefetch_l2)
+    prefetch_l2(x + rw.r0 * hidden,
+                (uint32_t)((n < kPrefetchRows ? n : kPrefetchRows) * row_bytes));
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -389,6 +397,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma(
   // the next kernel (the dw finalize) may be scheduled now; it waits for
   // this grid to complete before reading the partials
   pdl_trigger();
+  if (threadIdx.x == 0 && n > 0) {  // the first rows into L2 (prefetch_l2)
+    const uint32_t b = (uint32_t)((n < kPrefetchRows ? n : kPrefetchRows) * row_bytes);
+    prefetch_l2(x + rw.r0 * hidden, b);
+    prefetch_l2(dy + rw.r0 * hidden, b);
+  }
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -563,6 +576,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma_rows(
   }
   __syncthreads();
   pdl_trigger();
+  if (threadIdx.x == 0 && n > 0) {  // the first stages into L2 (prefetch_l2)
+    const int pr = n < kPrefetchRows * K ? n : kPrefetchRows * K;
+    const uint32_t b = (uint32_t)(pr * row_bytes);
+    prefetch_l2(x + rw.r0 * hidden, b);
+    prefetch_l2(dy + rw.r0 * hidden, b);
+  }
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -824,6 +843,11 @@ __global__ void __launch_bounds__(VPT == 2 ? kLnBwd2Threads : kMaxThreads, 1) ln
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
   pdl_trigger();
+  if (threadIdx.x == 0 && n > 0) {  // the first rows into L2 (prefetch_l2)
+    const uint32_t b = (uint32_t)((n < kPrefetchRows ? n : kPrefetchRows) * row_bytes);
+    prefetch_l2(x + rw.r0 * hidden, b);
+    prefetch_l2(dy + rw.r0 * hidden, b);
+  }
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1569,6 +1593,11 @@ __global__ void __launch_bounds__(kWideThreads, 1) fwd_tma_split(
   __syncthreads();
   cluster_sync();  // the peers' barriers are initialised
   pdl_trigger();
+  if (threadIdx.x == 0) {  // the first rows' slices into L2 (prefetch_l2)
+    const int64_t c0 = (int64_t)rank * part;
+    for (int i = 0; i < n && i < kPrefetchRows; ++i)
+      prefetch_l2(x + rw.row(i) * hidden + c0, (uint32_t)part_bytes);
+  }
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
