@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(256) sm_fwd_warp_rows(const T* __restrict__ x,
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_trigger();
   if (row >= rows) return;  // whole warps leave together
+  if (lane == 0) prefetch_l2(x + row * cols, (uint32_t)(cols * sizeof(T)));
   pdl_wait();
   const int nvec = cols / E;
   const T* xr = x + row * cols;
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) sm_fwd_cta_row(
   const int nvec = cols / E;
   const T* xr = x + row * cols;
   pdl_trigger();
+  if (threadIdx.x == 0) prefetch_l2(xr, (uint32_t)(cols * sizeof(T)));
   pdl_wait();
   uint4 xv[VPT];
 #pragma unroll
@@ -246,6 +248,10 @@ __global__ void __launch_bounds__(256) sm_bwd_warp_rows(const T* __restrict__ dy
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_trigger();
   if (row >= rows) return;
+  if (lane == 0) {
+    prefetch_l2(y + row * cols, (uint32_t)(cols * sizeof(T)));
+    prefetch_l2(dy + row * cols, (uint32_t)(cols * sizeof(T)));
+  }
   pdl_wait();
   const int nvec = cols / E;
   uint4 yv[VPT], dv[VPT];
@@ -273,6 +279,10 @@ __global__ void __launch_bounds__(VPT >= 8 ? 512 : 1024) sm_bwd_cta_row(
   const int64_t row = blockIdx.x;
   const int nvec = cols / E;
   pdl_trigger();
+  if (threadIdx.x == 0) {
+    prefetch_l2(y + row * cols, (uint32_t)(cols * sizeof(T)));
+    prefetch_l2(dy + row * cols, (uint32_t)(cols * sizeof(T)));
+  }
   pdl_wait();
   uint4 yv[VPT], dv[VPT];
 #pragma unroll
@@ -307,6 +317,11 @@ __global__ void __launch_bounds__(1024) sm_bwd_rows(const T* __restrict__ dy,
   const int64_t r0 = (int64_t)blockIdx.x * rows / gridDim.x;
   const int64_t r1 = (int64_t)(blockIdx.x + 1) * rows / gridDim.x;
   pdl_trigger();
+  if (threadIdx.x == 0 && r1 > r0) {  // the first rows into L2 (prefetch_l2)
+    const uint32_t b = (uint32_t)((r1 - r0 < 4 ? r1 - r0 : 4) * cols * (int64_t)sizeof(T));
+    prefetch_l2(y + r0 * cols, b);
+    prefetch_l2(dy + r0 * cols, b);
+  }
   pdl_wait();
   auto load = [&](int64_t r, uint4& yb, uint4& db) {
     yb = in ? ld_stream(y + r * cols + (int64_t)v * E) : make_uint4(0, 0, 0, 0);
