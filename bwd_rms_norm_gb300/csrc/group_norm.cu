@@ -400,6 +400,9 @@ __global__ void __launch_bounds__(kGnThreadsMax, 1) gn_fwd_pipe(
   __syncthreads();
   if (csize > 1) cluster_sync();  // peers' barriers are initialised
   pdl_trigger();
+  if (threadIdx.x == 0)  // the first slices into L2 (prefetch_l2)
+    for (int i = 0; i < count && i < 2; ++i)
+      prefetch_l2(x + (g0 + i) * M + (int64_t)rank * nv * E, sb);
   pdl_wait();
   volatile int* abort = &pp.abort;
   const int vbase = (int)rank * nv;  // first vector of this CTA's slice
@@ -620,6 +623,12 @@ __global__ void __launch_bounds__(kL2Threads, 1) gn_bwd_l2(
   __syncthreads();
   if (csize > 1) cluster_sync();
   pdl_trigger();
+  if (threadIdx.x == 0 && count > 0) {  // the first chunks into L2 (prefetch_l2)
+    const int64_t off = g0 * M + (int64_t)vbase * E;
+    const uint32_t b = (uint32_t)(nv < stages * CH ? nv : stages * CH) * 16u;
+    prefetch_l2(x + off, b);
+    prefetch_l2(dy + off, b);
+  }
   pdl_wait();
   volatile int* abort = &st.abort;
 
