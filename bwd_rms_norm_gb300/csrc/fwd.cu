@@ -273,11 +273,12 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t s, int* launches) {
 
 // Kernel choice by row width (measured on GB300 with the workloads of the
 // tests, as forward+backward steps): rows over 4 KB run the staged TMA
-// pipeline where its ring and registers hold them -- one persistent CTA per
-// SM hands the SMs to the next kernel with less turnover than one CTA per
-// row, which made whole steps 2-9% faster although the forward alone is up
-// to 9% slower on the widest rows -- and rows up to 4 KB run the register
-// kernels.  Rows too wide for both are split over a thread-block cluster.
+// pipeline -- one persistent CTA per SM (fwd_tma), or a cluster of 2 or 4
+// CTAs per row range for rows its ring and registers cannot hold
+// (fwd_tma_split) -- which hands the SMs to the next kernel with less
+// turnover than one CTA per row; rows up to 4 KB run the register kernels.
+// Rows too wide for all of these (fp32 65536) are held in the registers of
+// a thread-block cluster (fwd_cluster).
 cudaError_t launch_fwd(int dtype, const FwdArgs& a, cudaStream_t s, int* launches) {
   cudaError_t e = cudaSuccess;
   const int row_bytes = a.hidden * (dtype == 0 ? 4 : 2);
