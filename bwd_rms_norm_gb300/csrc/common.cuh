@@ -291,8 +291,8 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* red, int 
 // (steps of forward + backward): 16384 x 8192 bf16 6502 -> 6596 GB/s
 // (backward 121.3 -> 119.3 us), 4096 x 4096 bf16 4911 -> 5107 GB/s
 // (backward 19.59 -> 18.60 us), 4096 x 1024 fp16 backward 9.10 -> 8.01 us;
-// calls made alone unchanged.  Slower, and so left out: the LayerNorm
-// forward, the wide and the split backward.
+// calls made alone unchanged.  The wide and split backward, whose rows are
+// 32-64 KB, prefetch one row: a whole ring was slower there.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }

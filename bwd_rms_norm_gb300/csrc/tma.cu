@@ -715,6 +715,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) ln_fwd_tma(
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
   pdl_trigger();
+  if (threadIdx.x == 0 && n > 0)  // the first rows into L2 (prefetch_l2)
+    prefetch_l2(x + rw.r0 * hidden,
+                (uint32_t)((n < kPrefetchRows ? n : kPrefetchRows) * row_bytes));
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1022,6 +1025,11 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_wide(
   }
   __syncthreads();
   pdl_trigger();
+  // the first row into L2 (prefetch_l2; one row: a whole ring was slower)
+  if (threadIdx.x == 0 && n > 0) {
+    prefetch_l2(x + rw.r0 * hidden, (uint32_t)row_bytes);
+    prefetch_l2(dy + rw.r0 * hidden, (uint32_t)row_bytes);
+  }
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1327,6 +1335,13 @@ __global__ void __launch_bounds__(kWideThreads, 1) bwd_tma_split(
   __syncthreads();
   cluster_sync();  // the peers' barriers are initialised
   pdl_trigger();
+  // the first row's slices into L2 (prefetch_l2; one row: a whole ring was
+  // slower)
+  if (threadIdx.x == 0 && n > 0) {
+    const int64_t c0 = (int64_t)rank * part;
+    prefetch_l2(x + rw.row(0) * hidden + c0, (uint32_t)part_bytes);
+    prefetch_l2(dy + rw.row(0) * hidden + c0, (uint32_t)part_bytes);
+  }
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
