@@ -652,6 +652,9 @@ def run_ours(args, rank, world, local):
     fwd_ach = w.fwd_bytes() / (fwd_us * 1e-6) / 1e9
     bwd_ach = w.bwd_bytes() / (bwd_us * 1e-6) / 1e9
     traffic = load_traffic(args.workload)
+    if dp_info is not None:
+        # the capture covers rms_norm_bwd, not the fixed-block backward
+        traffic = {k: v for k, v in traffic.items() if k != "bwd"}
     iso = isolated_calls(fwd, bwd, nsets, dev, l2)
 
     # end to end through the public API: pinned host inputs in, results out
