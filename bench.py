@@ -3,9 +3,10 @@
 
 One step = one forward (rms_norm_fwd) and one backward (rms_norm_bwd, which
 includes the fixed-order weight-gradient reduction) over one batch of the
-workload, through the C ABI.  Default workload: Llama-shaped bf16
-activation, 4096 rows (4 x 1024 tokens) x hidden 4096, eps 1e-5, round-once
-store, inputs drawn once (seeded) and resident in HBM.
+workload, through the C ABI.  Default workload: a bf16 activation of 16384
+rows x hidden 8192, eps 1e-5, round-once store, inputs drawn once (seeded)
+and resident in HBM; ``--workload`` picks another (the round-twice store on
+the same shape, the Llama-shaped 4096 x 4096, the fp16 width sweep, ...).
 
 Timing.  The batch is copied several times in HBM (at least six L2 sizes
 of data in all) and the steps cycle through the copies, the backward of a
