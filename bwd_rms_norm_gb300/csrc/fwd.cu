@@ -63,7 +63,7 @@ __device__ __forceinline__ void store_vec(void* y, int64_t elem,
     for (int i = 0; i < E; ++i) o[i] = ((xf[i] * rs) * (gf[i] + off)) * sc;
     st_e4m3<E>(static_cast<unsigned char*>(y) + elem, o);
   } else {
-    st_vec(static_cast<T*>(y) + elem, scale_vec<T>(xf, gv, rs, off, twice));
+    st_vec_stream(static_cast<T*>(y) + elem, scale_vec<T>(xf, gv, rs, off, twice));
   }
 }
 

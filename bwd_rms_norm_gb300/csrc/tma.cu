@@ -105,6 +105,53 @@ __device__ __forceinline__ Rows cta_rows(int64_t rows) {
   return r;
 }
 
+// The rows of a forward CTA dealt round-robin (a forward keeps no row
+// order: every row's outputs are its own): its i-th row is r0 + i * step,
+// r0 the CTA's index and step the grid, so that the grid streams one window
+// of consecutive rows at a time.  The forwards take it for rows of
+// kRoundRobinBytes and more (a template switch; narrower rows keep the
+// contiguous split).  Measured on GB300 (forward alone, and steps of forward
+// + backward): 16384 x 8192 bf16 87.0 -> 85.6 us (step 201.3 -> 200.3 us),
+// its LayerNorm 92.9 -> 88.6 us (step 221.1 -> 217.1 us), 4096 x 16384 fp16
+// 44.4 -> 43.0 us (step 106.8 -> 105.6 us); slower for 6 KB rows (8192 x
+// 3072 bf16 17.31 -> 17.56 us) and under the FP8 store (16384 x 8192
+// 63.2 -> 64.1 us).
+struct StridedRows {
+  int64_t r0, step;
+  int n;
+  __device__ __forceinline__ int64_t row(int i) const { return r0 + (int64_t)i * step; }
+};
+
+constexpr int kRoundRobinBytes = 16 * 1024;
+
+template <bool RR>
+__device__ __forceinline__ std::conditional_t<RR, StridedRows, Rows> fwd_rows(int64_t rows) {
+  if constexpr (RR) {
+    StridedRows r;
+    r.r0 = blockIdx.x;
+    r.step = gridDim.x;
+    r.n = (int)((rows - blockIdx.x + gridDim.x - 1) / gridDim.x);
+    return r;
+  } else {
+    return cta_rows(rows);
+  }
+}
+
+// The CTA's first rows of x into L2 (prefetch_l2): one hint over a
+// contiguous range, one a row when they are dealt round-robin.
+template <typename T>
+__device__ __forceinline__ void prefetch_first_rows(const T* x, const Rows& rw, int hidden) {
+  if (rw.n > 0)
+    prefetch_l2(x + rw.r0 * hidden,
+                (uint32_t)((rw.n < kPrefetchRows ? rw.n : kPrefetchRows) * hidden * sizeof(T)));
+}
+
+template <typename T>
+__device__ __forceinline__ void prefetch_first_rows(const T* x, const StridedRows& rw, int hidden) {
+  for (int q = 0; q < rw.n && q < kPrefetchRows; ++q)
+    prefetch_l2(x + rw.row(q) * hidden, (uint32_t)(hidden * sizeof(T)));
+}
+
 // Position in the ring: stage index and phase parity, advanced without
 // division.
 struct RingPos {
@@ -136,9 +183,9 @@ __device__ __forceinline__ void init_pipe(Pipe& p, int stages, int applier_warps
 // into the ring.  NSRC source tensors go to consecutive parts of a stage.
 // Rows are `pitch` bytes apart in global memory; `bytes` of each are copied
 // (a whole row, or the slice a CTA of a cluster owns).
-template <int NSRC>
+template <int NSRC, class RW = Rows>
 __device__ void produce_pitched(Pipe& p, unsigned char* ring, int stride, int stages,
-                                const void* const (&src)[NSRC], const Rows& rw, size_t pitch,
+                                const void* const (&src)[NSRC], const RW& rw, size_t pitch,
                                 uint32_t bytes, volatile int* abort) {
   RingPos pos{0, 0u};
   int i = 0;
@@ -169,11 +216,11 @@ __device__ void produce_pitched(Pipe& p, unsigned char* ring, int stride, int st
   }
 }
 
-template <int NSRC>
+template <int NSRC, class RW = Rows>
 __device__ __forceinline__ void produce(Pipe& p, unsigned char* ring, int stride, int stages,
-                                        const void* const (&src)[NSRC], const Rows& rw,
+                                        const void* const (&src)[NSRC], const RW& rw,
                                         uint32_t row_bytes, volatile int* abort) {
-  produce_pitched<NSRC>(p, ring, stride, stages, src, rw, row_bytes, row_bytes, abort);
+  produce_pitched<NSRC, RW>(p, ring, stride, stages, src, rw, row_bytes, row_bytes, abort);
 }
 
 // Producer of stages that hold K consecutive rows each (narrow rows): stage
@@ -245,8 +292,9 @@ __device__ __forceinline__ void stage_gains(float* gain, const T* __restrict__ g
 
 // Forward.  Reducer: sum of squares of its row, rstd, written to global and
 // to the stage's slot.  Appliers: y = round((x * rstd) * gain) (or the
-// round-twice store) for their vectors of every row.
-template <typename T, int VPT, bool F8>
+// round-twice store) for their vectors of every row.  RR: rows dealt
+// round-robin (StridedRows).
+template <typename T, int VPT, bool F8, bool RR>
 __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
     const T* __restrict__ x, const T* __restrict__ gamma, void* __restrict__ y,
     float* __restrict__ rstd, int64_t rows, int hidden, float eps, float off, int twice,
@@ -257,14 +305,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) fwd_tma(
   const int row_bytes = hidden * (int)sizeof(T);
   const int stride = (row_bytes + 127) / 128 * 128;
   const int appliers = blockDim.x - 32 * (1 + reducers);
-  const Rows rw = cta_rows(rows);
+  const auto rw = fwd_rows<RR>(rows);
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
   pdl_trigger();
-  if (threadIdx.x == 0 && n > 0)  // the first rows into L2 (prefetch_l2)
-    prefetch_l2(x + rw.r0 * hidden,
-                (uint32_t)((n < kPrefetchRows ? n : kPrefetchRows) * row_bytes));
+  if (threadIdx.x == 0) prefetch_first_rows(x, rw, hidden);
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -699,7 +745,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) bwd_tma_rows(
 // the stage (two passes over shared memory), rstd; both to global and to
 // the stage's slots.  Appliers: y = round(fma((x - mean) * rstd, gamma,
 // beta)), gains and biases kept packed in registers and widened at use.
-template <typename T, int VPT>
+// RR: rows dealt round-robin, as in fwd_tma.
+template <typename T, int VPT, bool RR>
 __global__ void __launch_bounds__(kMaxThreads, 1) ln_fwd_tma(
     const T* __restrict__ x, const T* __restrict__ gamma, const T* __restrict__ beta,
     T* __restrict__ y, float* __restrict__ mean, float* __restrict__ rstd, int64_t rows,
@@ -710,14 +757,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) ln_fwd_tma(
   const int row_bytes = hidden * (int)sizeof(T);
   const int stride = (row_bytes + 127) / 128 * 128;
   const int appliers = blockDim.x - 32 * (1 + reducers);
-  const Rows rw = cta_rows(rows);
+  const auto rw = fwd_rows<RR>(rows);
   const int n = rw.n;
   init_pipe(pipe, stages, appliers / 32);
   __syncthreads();
   pdl_trigger();
-  if (threadIdx.x == 0 && n > 0)  // the first rows into L2 (prefetch_l2)
-    prefetch_l2(x + rw.r0 * hidden,
-                (uint32_t)((n < kPrefetchRows ? n : kPrefetchRows) * row_bytes));
+  if (threadIdx.x == 0) prefetch_first_rows(x, rw, hidden);
   pdl_wait();
   volatile int* abort = &pipe.abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1223,7 +1268,10 @@ int grid_for(int64_t rows, int64_t cap, cudaError_t* err) {
 template <typename T, int VPT, bool F8>
 cudaError_t launch_fwd_tma_vf(const FwdArgs& a, int appliers, int stages, int reducers, int grid,
                               cudaStream_t s) {
-  auto kern = fwd_tma<T, VPT, F8>;
+  auto kern = fwd_tma<T, VPT, F8, false>;
+  // rows of 16 KB and more need two vectors an applier at least
+  if constexpr (VPT >= 2 && !F8)
+    if (a.hidden * (int)sizeof(T) >= kRoundRobinBytes) kern = fwd_tma<T, VPT, F8, true>;
   const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   cudaError_t e = allow_smem((const void*)kern);
   if (e != cudaSuccess) return e;
@@ -1887,7 +1935,9 @@ bool try_bwd_tma_t(const BwdArgs& a, cudaStream_t s, cudaError_t* err, int64_t* 
 template <typename T, int VPT>
 cudaError_t launch_ln_fwd_tma_v(const LnFwdArgs& a, int appliers, int stages, int reducers,
                                 int grid, cudaStream_t s) {
-  auto kern = ln_fwd_tma<T, VPT>;
+  auto kern = ln_fwd_tma<T, VPT, false>;
+  if constexpr (VPT >= 2)
+    if (a.hidden * (int)sizeof(T) >= kRoundRobinBytes) kern = ln_fwd_tma<T, VPT, true>;
   const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   cudaError_t e = allow_smem((const void*)kern);
   if (e != cudaSuccess) return e;

@@ -60,6 +60,29 @@ def test_rms_norm_dispatch(L, name, fwd, bwd):
     _expect(_kernels(L), fwd)
 
 
+def test_staged_forwards_deal_wide_rows_round_robin(L):
+    """The staged forwards take the CTA's rows round-robin for rows of 16 KB
+    and more (the last template argument, RR), contiguous ranges for
+    narrower rows and under the FP8 store (F8, the one before it)."""
+    sc = torch.tensor([8.0], device="cuda")
+    for name, plain, fp8 in (("large_bf16_16384x8192_once", "Lb0ELb1EE", "Lb1ELb0EE"),
+                             ("fp16_4096x16384", "Lb0ELb1EE", "Lb1ELb0EE"),
+                             ("llama_bf16_4096x4096", "Lb0ELb0EE", "Lb1ELb0EE"),
+                             ("gemma_bf16_8192x3072", "Lb0ELb0EE", "Lb1ELb0EE")):
+        w = W.all_workloads()[name]
+        t = _dev(w, rows=300)
+        L.rms_norm_fwd(t["x"], t["gamma"], w.eps, w.offset, w.cast_mode)
+        _expect(_kernels(L), plain)
+        L.rms_norm_fwd_fp8(t["x"], t["gamma"], sc, w.eps, w.offset)
+        _expect(_kernels(L), fp8)
+    for name, part in (("ln_bf16_16384x8192", "ln_fwd_tmaI13__nv_bfloat16Li2ELb1EE"),
+                       ("ln_bf16_4096x4096", "ln_fwd_tmaI13__nv_bfloat16Li1ELb0EE")):
+        w = W.layer_norm_workloads()[name]
+        t = _dev(w, rows=300)
+        L.layer_norm_fwd(t["x"], t["gamma"], t["beta"], w.eps)
+        _expect(_kernels(L), part)
+
+
 def test_unaligned_rows_take_the_scalar_kernels(L):
     x = torch.randn(8, 1001, device="cuda").to(torch.bfloat16)
     g = torch.ones(1001, device="cuda", dtype=torch.bfloat16)
