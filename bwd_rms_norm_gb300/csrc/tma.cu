@@ -5,16 +5,16 @@
 // write any output of a row before the whole row has been reduced, so two
 // things decide the speed: how many bytes each SM keeps in flight, and that
 // the latency of each row's reduction never stalls the stream of outputs.
-// One CTA per SM owns a contiguous range of rows (rows too wide for one
-// CTA's ring are split over a cluster of 2 or 4 CTAs, each staging its part
-// of every row) and splits its warps into three roles that meet at
-// per-stage mbarriers:
+// One CTA per SM owns a contiguous range of rows (in the forwards of rows of
+// 16 KB and more, every grid-th row; rows too wide for one CTA's ring are
+// split over a cluster of 2 or 4 CTAs, each staging its part of every row)
+// and splits its warps into three roles that meet at per-stage mbarriers:
 //
 //   producer (warp 0, one thread)  streams the CTA's rows into a ring of
 //       shared-memory stages with 1D bulk copies (cp.async.bulk, the TMA
 //       engine) -- up to 96 KB of rows in flight per SM in the forward of
-//       rows up to 16 KB, up to 200 KB otherwise, none of it held in
-//       registers;                                                -> full[s]
+//       rows up to 16 KB (but for the FP8 store of 16 KB rows), up to
+//       200 KB otherwise, none of it held in registers;          -> full[s]
 //   reducers (warps 1..R)  one warp per row (warp d takes the CTA's rows
 //       d, d + R, ...): the row statistic -- rstd in the forward,
 //       c = sum(g * x_hat) / hidden in the backward -- into the stage's slot;
@@ -114,8 +114,8 @@ __device__ __forceinline__ Rows cta_rows(int64_t rows) {
 // + backward): 16384 x 8192 bf16 87.0 -> 85.6 us (step 201.3 -> 200.3 us),
 // its LayerNorm 92.9 -> 88.6 us (step 221.1 -> 217.1 us), 4096 x 16384 fp16
 // 44.4 -> 43.0 us (step 106.8 -> 105.6 us); slower for 6 KB rows (8192 x
-// 3072 bf16 17.31 -> 17.56 us) and under the FP8 store (16384 x 8192
-// 63.2 -> 64.1 us).
+// 3072 bf16 17.31 -> 17.56 us).  Under the FP8 store only with the full
+// ring (kFwdRingBytes).
 struct StridedRows {
   int64_t r0, step;
   int n;
@@ -1253,7 +1253,12 @@ void split_stages(int fit, int* stages, int* reducers) {
 // flight a CTA.  Measured on GB300, deeper rings slow the forward (more
 // reads in flight beside its stores): 4096 x 4096 bf16 0.785 of the copy
 // bandwidth with 24 stages, 0.809 with 12; 16384 x 8192 bf16 0.877 with 12
-// stages, 0.903 with 6; its FP8 forward 0.887 with 12, 0.92 with 6.
+// stages, 0.903 with 6; its FP8 forward 0.887 with 12, 0.92 with 6.  The
+// FP8 forward of rows of 16 KB, whose rows go round-robin, takes the full
+// ring: 16384 x 8192 bf16 63.3 -> 59.4 us (steps 183.1 -> 178.7 us),
+// where the full ring alone gained 0.4 % and round-robin rows alone lost
+// 1.4 %; narrower FP8 rows keep kFwdRingBytes (4096 x 4096 bf16 10.75
+// against 11.12 us with the full ring).
 constexpr int kFwdRingBytes = 96 * 1024;
 
 int grid_for(int64_t rows, int64_t cap, cudaError_t* err) {
@@ -1270,7 +1275,7 @@ cudaError_t launch_fwd_tma_vf(const FwdArgs& a, int appliers, int stages, int re
                               cudaStream_t s) {
   auto kern = fwd_tma<T, VPT, F8, false>;
   // rows of 16 KB and more need two vectors an applier at least
-  if constexpr (VPT >= 2 && !F8)
+  if constexpr (VPT >= 2)
     if (a.hidden * (int)sizeof(T) >= kRoundRobinBytes) kern = fwd_tma<T, VPT, F8, true>;
   const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   cudaError_t e = allow_smem((const void*)kern);
@@ -1296,7 +1301,9 @@ bool try_fwd_tma_t(const FwdArgs& a, cudaStream_t s, cudaError_t* err) {
   constexpr int E = Traits<T>::kVec;
   const int stride = (a.hidden * (int)sizeof(T) + 127) / 128 * 128;
   int stages = 0, reducers = 0;
-  split_stages((stride <= 16 * 1024 ? kFwdRingBytes : kRingBudget) / stride, &stages,
+  const bool full_ring = stride > 16 * 1024 ||
+                         (a.fp8 && a.hidden * (int)sizeof(T) >= kRoundRobinBytes);
+  split_stages((full_ring ? kRingBudget : kFwdRingBytes) / stride, &stages,
                &reducers);
   // rows too wide for this kernel go over a cluster (fwd_tma_split)
   if (stages < 3) return try_fwd_split_t<T>(a, s, err);

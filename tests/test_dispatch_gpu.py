@@ -62,11 +62,11 @@ def test_rms_norm_dispatch(L, name, fwd, bwd):
 
 def test_staged_forwards_deal_wide_rows_round_robin(L):
     """The staged forwards take the CTA's rows round-robin for rows of 16 KB
-    and more (the last template argument, RR), contiguous ranges for
-    narrower rows and under the FP8 store (F8, the one before it)."""
+    and more (the last template argument, RR; the one before it is F8, the
+    FP8 store), contiguous ranges for narrower rows."""
     sc = torch.tensor([8.0], device="cuda")
-    for name, plain, fp8 in (("large_bf16_16384x8192_once", "Lb0ELb1EE", "Lb1ELb0EE"),
-                             ("fp16_4096x16384", "Lb0ELb1EE", "Lb1ELb0EE"),
+    for name, plain, fp8 in (("large_bf16_16384x8192_once", "Lb0ELb1EE", "Lb1ELb1EE"),
+                             ("fp16_4096x16384", "Lb0ELb1EE", "Lb1ELb1EE"),
                              ("llama_bf16_4096x4096", "Lb0ELb0EE", "Lb1ELb0EE"),
                              ("gemma_bf16_8192x3072", "Lb0ELb0EE", "Lb1ELb0EE")):
         w = W.all_workloads()[name]
