@@ -114,8 +114,8 @@ __device__ __forceinline__ Rows cta_rows(int64_t rows) {
 // + backward): 16384 x 8192 bf16 87.0 -> 85.6 us (step 201.3 -> 200.3 us),
 // its LayerNorm 92.9 -> 88.6 us (step 221.1 -> 217.1 us), 4096 x 16384 fp16
 // 44.4 -> 43.0 us (step 106.8 -> 105.6 us); slower for 6 KB rows (8192 x
-// 3072 bf16 17.31 -> 17.56 us).  Under the FP8 store only with the full
-// ring (kFwdRingBytes).
+// 3072 bf16 17.31 -> 17.56 us).  Under the FP8 store they pay only
+// together with the full ring (see kFwdRingBytes).
 struct StridedRows {
   int64_t r0, step;
   int n;
